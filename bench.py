@@ -1,0 +1,364 @@
+"""Decode-step benchmark of the CONF-KV cache manager on GB300.
+
+One step = the whole decode-step path for all sequences and layers:
+confidence reduction + ring append, mixed FP16/INT8 attention with attention
+mass, and select / compact / requantise.  The default workload is the
+Qwen-32B-shaped one (64 layers, 40/8 heads, d 128, vocab 152064, batch 8,
+4096-token prefill, N_high 1024 / N_low 2048, P 64, W 256).
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs an independent
+replica of the workload (sequences are independent: no collective on the
+data path); `value` is the whole-job step rate.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference   # the float64 CPU oracle on host cores
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "CONF-KV decode steps/s (all layers) + achieved HBM GB/s vs GB300 peak, 1 GPU"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            return float(d["hbm_gbs"]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def _traffic_from_profiles(kernel_tag: str):
+    """Per-launch DRAM bytes of a kernel from a committed ncu summary line
+    `dram_bytes_per_launch: <int>` of profiles/<kernel_tag>.md, if present."""
+    p = os.path.join(ROOT, "profiles", kernel_tag + ".md")
+    if not os.path.exists(p):
+        return None
+    for line in open(p):
+        if line.strip().startswith("dram_bytes_per_launch:"):
+            try:
+                return float(line.split(":", 1)[1].strip().split()[0])
+            except ValueError:
+                return None
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) >= 9:
+                rows.append(f)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = sorted(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
+        mx = max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit())
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx, "reasons": reasons,
+                "samples": len(rows)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class OracleSample:
+    """The float64 oracle over a bounded sample of the workload: `units`
+    (sequence, layer) units, each prefilled and stepped once during set-up
+    (the first step evicts the prefill down to the budget), then stepped at
+    steady-state cache size by `run`."""
+
+    def __init__(self, w, seed: int, units: int):
+        import numpy as np
+        from oracle import confkv_oracle as orc
+        from workload import prefill_unit
+        self.w, self.seed, self.orc = w, seed, orc
+        self.prm = orc.Params.from_workload(w)
+        rng = np.random.default_rng(seed)
+        self.picks = [(int(rng.integers(w.B)), int(rng.integers(w.L))) for _ in range(units)]
+        self.states = []
+        self.s = 0
+        for b, l in self.picks:
+            k, v = prefill_unit(w, seed, b, l)
+            self.states.append(orc.prefill_unit(k, v, w.W))
+        self.run(1)
+
+    def run(self, steps: int):
+        from workload import step_unit, step_logits
+        orc, w = self.orc, self.w
+        done = 0
+        wall0, cpu0 = time.perf_counter(), time.process_time()
+        for _ in range(steps):
+            for i, (b, l) in enumerate(self.picks):
+                q, kn, vn = step_unit(w, self.seed, self.s, b, l)
+                c = orc.confidence(step_logits(w, self.seed, self.s, b)).c
+                N = orc.budget(c, w.tau, w.n_high[l], w.n_low[l])
+                self.states[i] = orc.step_unit(self.prm, self.states[i], w.T0 + self.s,
+                                               q.float().numpy(), kn, vn, N).state
+                done += 1
+            self.s += 1
+        return done, time.perf_counter() - wall0, time.process_time() - cpu0
+
+    def steps_per_s(self, done: int, wall: float) -> float:
+        return 1.0 / (wall / max(done, 1) * self.w.L * self.w.B)
+
+
+def cpu_baseline(w, seed: int, units: int = 8, steps: int = 24):
+    """Oracle steps/s of the whole workload, extrapolated from a bounded
+    sample of unit-steps timed on the host cores."""
+    smp = OracleSample(w, seed, units)
+    done, wall, cpu = smp.run(steps)
+    return {
+        "value": smp.steps_per_s(done, wall),
+        "unit": "steps/s",
+        "cores": max(1, int(round(cpu / wall))) if wall > 0 else 1,
+        "cores_available": len(os.sched_getaffinity(0)),
+        "kind": "oracle",
+        "sample": "%d (sequence, layer) unit-steps of %s at steady-state cache size (confidence "
+                  "over the full vocabulary, attention, EMA, ranking, eviction, requantisation), "
+                  "%.1f s wall; steps/s = 1 / (time per unit-step x L x B)" % (done, w.name, wall),
+    }
+
+
+def run_reference(args):
+    from workload import get_workload
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    w = get_workload(args.workload)
+    smp = OracleSample(w, args.seed, units=2)
+    for _ in range(args.warmup):
+        smp.run(1)
+    vals = []
+    tot_done, tot_wall, tot_cpu = 0, 0.0, 0.0
+    for _ in range(args.steps):
+        done, wall, cpu = smp.run(1)
+        vals.append(smp.steps_per_s(done, wall))
+        tot_done += done
+        tot_wall += wall
+        tot_cpu += cpu
+    vals.sort()
+    v = vals[len(vals) // 2]
+    cpu_line = {"value": v, "unit": "steps/s",
+                "cores": max(1, int(round(tot_cpu / tot_wall))) if tot_wall > 0 else 1,
+                "cores_available": len(os.sched_getaffinity(0)), "kind": "oracle",
+                "sample": "each step: 2 (sequence, layer) unit-steps of %s at steady-state size; "
+                          "steps/s = 1 / (time per unit-step x L x B), median over steps" % w.name}
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / v,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "global_batch": w.B, "seq_len": w.T0,
+                                         "layers": w.L, "parallelism": "replicas"},
+        "cpu_baseline": cpu_line,
+        "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    ws, rank, local = _dist()
+    if ws > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import confidence_gated_kv_gb300 as ck
+    if not os.path.exists(ck.binding.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    from workload import get_workload, prefill_batch_fast, step_pool_fast
+
+    w = get_workload(args.workload)
+    seed = args.seed + 7919 * rank
+    cfg = ck.config_from_workload(w)
+    cache = ck.Cache(cfg, device=dev)
+    k, v = prefill_batch_fast(w, seed, dev)
+    cache.prefill(k, v, [w.T0] * w.B)
+    del k, v
+    R = args.pool
+    q, kn, vn, lg = step_pool_fast(w, seed, R, dev)
+    outs = cache.new_outputs()
+    stream = torch.cuda.current_stream()
+
+    for s in range(args.warmup):
+        cache.step(q[s % R], kn[s % R], vn[s % R], lg[s % R], outs)
+    torch.cuda.synchronize()
+    st0 = cache.stats()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    cache.profile_enable(args.steps)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for s in range(args.steps):
+        j = (args.warmup + s) % R
+        cache.step(q[j], kn[j], vn[j], lg[j], outs)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    ms = ev0.elapsed_time(ev1)
+    clk = clocks.stop()
+    prof = cache.profile_read()
+    cache.profile_disable()
+    st1 = cache.stats()
+
+    t = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if ws > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    steps_per_s = ws * args.steps / (ms_max / 1000.0)
+
+    attn_bytes = (st1["attn_bytes"] - st0["attn_bytes"]) / args.steps
+    step_bytes = (st1["step_bytes"] - st0["step_bytes"]) / args.steps
+    attn_ms = prof["attention_ms"] / max(prof["steps"], 1)
+    peak, peak_kind = _peaks()
+    achieved = attn_bytes / (attn_ms / 1000.0) / 1e9
+    traffic = _traffic_from_profiles("attention_kernel_" + w.name)
+
+    # ------------------------------------------------ end to end, host buffers
+    e2e = None
+    if args.e2e_steps > 0:
+        hq = [q[j].cpu().pin_memory() for j in range(R)]
+        hk = [kn[j].cpu().pin_memory() for j in range(R)]
+        hv = [vn[j].cpu().pin_memory() for j in range(R)]
+        hl = [lg[j].cpu().pin_memory() for j in range(R)]
+        hout = cache.host_outputs()
+        h2d = hq[0].numel() * hq[0].element_size() + 2 * hk[0].numel() * 2 + hl[0].numel() * 4
+        d2h = sum(x.numel() * x.element_size() for x in hout.values())
+        torch.cuda.synchronize()
+        e0 = time.perf_counter()
+        for s in range(args.e2e_steps):
+            j = s % R
+            cache.step_host(hq[j], hk[j], hv[j], hl[j], hout)
+        e_el = time.perf_counter() - e0
+        e2e = {"value": ws * args.e2e_steps / e_el, "unit": "steps/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "api": "confkv_step_host", "steps": args.e2e_steps}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, args.seed)
+
+    splits, smem = cache.attention_plan()
+    st = cache.stats()
+    if rank == 0:
+        line = {
+            "metric": METRIC,
+            "value": steps_per_s,
+            "unit": "steps/s",
+            "n_gpus": ws,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": ms_max / args.steps,
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "fp16/int8 storage, fp16 tensor-core products, fp32 accumulate",
+            "data": "synthetic",
+            "config": {"workload": w.name, "global_batch": w.B * ws, "seq_len": w.T0, "layers": w.L,
+                       "heads": [w.Hq, w.Hkv], "head_dim": w.d, "vocab": w.V,
+                       "budgets": [w.n_high[0], w.n_low[0]], "P": w.P, "W": w.W,
+                       "parallelism": "replicas (dp%d over sequences)" % ws,
+                       "l2": "per-step K/V stream %.2f GB > 129 MB L2, no flush" % (step_bytes / 1e9)},
+            "hbm": {"achieved_gbs": step_bytes / (ms_max / args.steps / 1000.0) / 1e9,
+                    "algorithmic_bytes_per_step": step_bytes, "peak_gbs": peak, "peak_kind": peak_kind,
+                    "frac": step_bytes / (ms_max / args.steps / 1000.0) / 1e9 / peak},
+            "roofline": {"kernel": "attention_kernel", "bound": "hbm", "achieved": achieved,
+                         "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                         "traffic": traffic, "algorithmic_bytes_per_launch": attn_bytes,
+                         "avg_launch_ms": attn_ms, "peak_kind": peak_kind},
+            "breakdown_ms_per_step": {k: prof[k + "_ms"] / max(prof["steps"], 1)
+                                      for k in ("prestep", "attention", "select")},
+            "attention_launch": {"ctas_per_unit": splits, "smem_bytes": smem},
+            "gpu_launches": 3 * args.steps,
+            "clocks": clk,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "state": {"resident_entries": st["resident"], "resident_kv_bytes": st["resident_bytes"],
+                      "evicted_total": st["evicted"], "moved_total": st["moved"]},
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=8)
+    ap.add_argument("--workload", default="qwen32b")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=4003)
+    ap.add_argument("--pool", type=int, default=16)
+    ap.add_argument("--e2e-steps", type=int, default=32)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

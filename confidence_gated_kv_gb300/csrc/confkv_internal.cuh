@@ -1,0 +1,152 @@
+// Internal definitions shared by the CONF-KV kernels and the host runtime.
+//
+// Data layout in HBM (all carved from one caller-allocated workspace):
+//
+//   Slot space of one (layer l, sequence b): S = cap + WR slots.
+//     slots [0, cap)       INT8 region, dense: slots [0, n8) are resident.
+//     slots [cap, cap+WR)  FP16 ring of WR = W + 16 slots; a token at
+//                          position p lives in ring slot p mod WR; a slot
+//                          whose pos is -1 is empty.
+//   Per-slot metadata [l][b][S]: pos (int32), ema (fp32).
+//   Attention-mass partials [l][b][kvh][S] (fp32, one per KV head).
+//
+//   K/V payload per unit u = (l, b, kvh), in 16-token blocks:
+//     INT8:  k8, v8  [u][cap/16][16*D bytes]
+//     FP16:  k16,v16 [u][WR/16][16*D halves]
+//   Inside a block the bytes are interleaved so that lane `lane` of a warp
+//   reading 16 contiguous bytes at  r*512 + lane*16  receives exactly its
+//   B-operand fragments of mma.m16n8k16 (QK^T for K, PV for V).  The
+//   offset functions below are the single definition of that interleave.
+#pragma once
+#include <cstdint>
+#include <cuda_fp16.h>
+
+namespace confkv {
+
+constexpr int kRingExtra = 16;      // WR = W + kRingExtra
+constexpr int kMaxG = 8;            // query heads per KV head supported
+constexpr int kMaxSV = 1024;        // confidence partial blocks per sequence
+
+// ---------------------------------------------------------------------------
+// Block interleave (host and device).  tau in [0,16) is the token within the
+// block, c in [0,D) the channel.  Returns a byte offset inside the block.
+// ---------------------------------------------------------------------------
+
+// INT8 K: token tau = 8*nt + g pairs with mma column g of n-tile nt; channel
+// c = 16*kk + {2t, 2t+1, 2t+8, 2t+9}[bsel] pairs with k-step kk, lane 4g+t.
+__host__ __device__ inline int k8_offset(int D, int tau, int c) {
+  int nt = tau >> 3, g = tau & 7;
+  int kk = c >> 4, cc = c & 15;
+  int t = (cc & 7) >> 1, bsel = ((cc >> 3) << 1) | (cc & 1);
+  int nc = D >> 5;                                // 16-byte chunks per lane
+  int r = nt * (nc >> 1) + (kk >> 2), w = kk & 3;
+  return r * 512 + ((g << 2) | t) * 16 + w * 4 + bsel;
+}
+
+// INT8 V: channel c = 8*j + g pairs with mma column g of n-tile j; token
+// tau = {2t, 2t+1, 2t+8, 2t+9}[bsel] pairs with the k index of lane 4g+t.
+__host__ __device__ inline int v8_offset(int D, int tau, int c) {
+  int j = c >> 3, g = c & 7;
+  int t = (tau & 7) >> 1, bsel = ((tau >> 3) << 1) | (tau & 1);
+  int r = j >> 2, w = j & 3;
+  (void)D;
+  return r * 512 + ((g << 2) | t) * 16 + w * 4 + bsel;
+}
+
+// FP16 K (offset in bytes): token tau = 8*nt + g; channel
+// c = 16*kk + 8*reg + 2t + half.
+__host__ __device__ inline int k16_offset(int D, int tau, int c) {
+  int nt = tau >> 3, g = tau & 7;
+  int kk = c >> 4, cc = c & 15;
+  int t = (cc & 7) >> 1, reg = cc >> 3, half = cc & 1;
+  int r = nt * (D >> 5) + (kk >> 1);
+  return r * 512 + ((g << 2) | t) * 16 + (kk & 1) * 8 + reg * 4 + half * 2;
+}
+
+// FP16 V (offset in bytes): channel c = 8*j + g; token
+// tau = 8*reg + 2t + half.
+__host__ __device__ inline int v16_offset(int D, int tau, int c) {
+  int j = c >> 3, g = c & 7;
+  int t = (tau & 7) >> 1, reg = tau >> 3, half = tau & 1;
+  int r = j >> 1;
+  (void)D;
+  return r * 512 + ((g << 2) | t) * 16 + (j & 1) * 8 + reg * 4 + half * 2;
+}
+
+// ---------------------------------------------------------------------------
+// Shapes, device pointers and counters passed to every kernel by value.
+// ---------------------------------------------------------------------------
+
+struct ConfPartial {     // one vocab chunk of one sequence
+  float M;               // chunk maximum
+  float z1, z2;          // largest and second largest logit of the chunk
+  int i1;                // index of z1 (lowest index on ties)
+  double S;              // sum exp(z - M)
+  double T;              // sum (z - M) exp(z - M)
+};
+
+struct DevStats {        // cumulative counters, updated with atomics
+  unsigned long long steps;
+  unsigned long long evicted;
+  unsigned long long moved;
+  unsigned long long requant;
+  unsigned long long attn_bytes;   // algorithmic bytes of the attention kernel
+  unsigned long long step_bytes;   // algorithmic bytes of the whole step
+};
+
+struct Shape {
+  int L, B, Hq, Hkv, G, D, V;
+  int cap, W, WR, P, S;      // S = cap + WR slots per (l, b)
+  int SV;                    // confidence partial blocks per sequence
+  int qbf16;                 // query dtype: 0 fp16, 1 bf16
+  int max_evict;             // rows of evicted_pos per (l, b)
+  double tau, wH, wm, wp;     // confidence weights and threshold (float64 math)
+  float alpha, lam;           // rank weight and EMA decay (float32 math)
+};
+
+struct Dev {
+  int8_t* k8;  int8_t* v8;
+  __half* k16; __half* v16;
+  float* sK;   float* sV;          // [l][b][kvh][D]
+  int32_t* pos; float* ema;        // [l][b][S]
+  float* mass;                     // [l][b][kvh][S]
+  int32_t* n8;                     // [l][b]
+  int32_t* T0;                     // [b]
+  int32_t* n_high; int32_t* n_low; // [l]
+  ConfPartial* conf;               // [b][SV]
+  uint32_t* scratch;               // [l][b][S] selection keys / compaction pairs
+  DevStats* stats;
+  int32_t* status;                 // device status word (0 = ok)
+  uint32_t* absmax;                // [2][l][b][kvh][D] prefill scratch
+};
+
+// Status bits written by kernels (never trap; the host reads them lazily).
+enum : int32_t {
+  kStatusOk = 0,
+  kStatusCapacity = 1,     // an INT8 region would overflow
+  kStatusEvictBound = 2,   // more evictions than the evicted_pos rows hold
+  kStatusBadCount = 4,     // inconsistent eviction count (selection failed)
+};
+
+__host__ __device__ inline size_t unit_index(const Shape& s, int l, int b, int h) {
+  return ((size_t)l * s.B + b) * s.Hkv + h;
+}
+__host__ __device__ inline size_t lb_index(const Shape& s, int l, int b) {
+  return (size_t)l * s.B + b;
+}
+
+// ---------------------------------------------------------------------------
+// Kernel launchers (defined in the .cu files; all asynchronous on `stream`).
+// ---------------------------------------------------------------------------
+int launch_prefill(const Shape& s, const Dev& d, const void* k, const void* v, long long t_max,
+                   const int32_t* T0_host, cudaStream_t stream);
+int launch_prestep(const Shape& s, const Dev& d, long long step, const float* logits,
+                   const void* k_new, const void* v_new, cudaStream_t stream);
+int launch_attention(const Shape& s, const Dev& d, const void* q, float* out, int splits,
+                     int max_tokens, cudaStream_t stream);
+int launch_select(const Shape& s, const Dev& d, long long step, int32_t* budget, float* conf_out,
+                  int32_t* evicted_pos, int32_t* n_evicted, int k_bound, cudaStream_t stream);
+int attention_smem_bytes(const Shape& s, int splits, int max_tokens);
+int attention_max_smem();
+
+}  // namespace confkv

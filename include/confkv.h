@@ -1,0 +1,233 @@
+/*
+ * confkv.h -- C ABI of the CONF-KV per-decode-step cache manager for one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The method: CONF-KV, "Confidence-Aware KV Cache Eviction with
+ * Mixed-Precision Storage for Long-Horizon LLM".  Citations name the page and
+ * the section they come from:
+ *   [rainbus]  paper.rainbus.top/paper/2605.24786 -- sections 核心方法 (core
+ *              method), 方法步骤详情 (Algorithm 1, steps 1-13), 前置知识
+ *              (prerequisites: EMA, blockwise online softmax), 复现评估
+ *              (reproducibility: hyper-parameters).
+ *   [gist-de]  gist.science/de/paper/2605.24786 -- Technischer
+ *              Zusammenfassung, Methodik: Konfidenzschätzung, Adaptive
+ *              Budgetauswahl, Token-Ranking und Eviktion, Systemintegration.
+ *
+ * Conventions
+ *   - Every function returns a status: CONFKV_OK (0) or a negative code below.
+ *     Nothing aborts, traps or exits the process.
+ *   - All tensor arguments of confkv_prefill / confkv_step are DEVICE
+ *     pointers owned by the caller; the library reads inputs and writes
+ *     outputs and keeps no reference after the call returns.  The only device
+ *     memory the library uses is the caller-allocated workspace (see
+ *     confkv_workspace_bytes); it never calls cudaMalloc itself.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Device work is enqueued on it and the call returns without
+ *     synchronising, except where a function says it synchronises.
+ *   - Device-side anomalies (an INT8 region that would overflow, an
+ *     inconsistent eviction count) set bits of a device status word; they are
+ *     reported as CONFKV_EDEVICE by the next confkv_get_stats.
+ *   - Layouts are row-major, outermost index first.  L layers, B sequences,
+ *     Hq query heads, Hkv KV heads, d head dim (64 or 128), V vocabulary.
+ */
+#ifndef CONFKV_H
+#define CONFKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CONFKV_OK 0
+#define CONFKV_EINVAL (-1)     /* bad argument or configuration */
+#define CONFKV_ECAPACITY (-2)  /* a cache region or output buffer is too small */
+#define CONFKV_ECUDA (-3)      /* a CUDA runtime call failed */
+#define CONFKV_ETIMEOUT (-4)   /* a bounded device wait gave up */
+#define CONFKV_ENOTIMPL (-5)   /* shape not supported by the compiled kernels */
+#define CONFKV_EDEVICE (-6)    /* the device status word reports an error */
+#define CONFKV_ESTATE (-7)     /* call out of order (e.g. step before prefill) */
+
+#define CONFKV_Q_FP16 0
+#define CONFKV_Q_BF16 1
+
+/*
+ * Configuration.  Defaults on the pages: w = (0.4, 0.3, 0.3) and tau = 0.7
+ * ([gist-de] Konfidenzschätzung; [rainbus] 核心方法), alpha = 0.65
+ * ([rainbus] 核心方法), lambda = 0.9 ([rainbus] 前置知识, EMA), P = 32 or 64,
+ * W = 128 ([rainbus] 复现评估).
+ */
+typedef struct confkv_config {
+  int32_t L, Hq, Hkv, d, V;   /* layers, query heads, KV heads, head dim, vocab */
+  int32_t B;                  /* sequences stepped together */
+  int32_t cap;                /* INT8 slots per (layer, sequence): must hold the
+                                 prefill older than W and every budget + 1;
+                                 rounded up to a multiple of 16 */
+  int32_t W;                  /* FP16 window: the newest W tokens stay FP16 */
+  int32_t P;                  /* protected window: the newest P tokens are never
+                                 evicted ([gist-de] Token-Ranking und Eviktion) */
+  int32_t q_dtype;            /* CONFKV_Q_FP16 or CONFKV_Q_BF16 */
+  int32_t max_evict;          /* rows of evicted_pos per (layer, sequence);
+                                 0 selects cap + W + 16 */
+  double tau;                 /* budget threshold: N = n_high if c >= tau */
+  double w_H, w_m, w_p;       /* confidence weights */
+  float alpha;                /* rank weight of the EMA mass */
+  float lam;                  /* EMA decay */
+  const int32_t* n_high;      /* host [L]: tight budget per layer (c >= tau) */
+  const int32_t* n_low;       /* host [L]: loose budget per layer (c < tau);
+                                 per-layer values give the pyramidal variant
+                                 ([gist-de] Systemintegration) */
+} confkv_config;
+
+typedef struct confkv_ctx confkv_ctx;
+
+/* Bytes of device workspace the context needs (state + scratch).  Returns
+ * CONFKV_EINVAL for an invalid configuration: d not 64/128, Hq % Hkv != 0,
+ * Hq / Hkv > 8, V < 2, some budget < P or < 1, cap < 16, W < 1. */
+int confkv_workspace_bytes(const confkv_config* cfg, size_t* bytes);
+
+/* Create a context over `workspace` (device memory, >= the size above, 256-byte
+ * aligned, owned by the caller and kept alive until confkv_destroy).  The
+ * context copies the configuration, including n_high / n_low.  Synchronous. */
+int confkv_create(const confkv_config* cfg, void* workspace, size_t workspace_bytes,
+                  confkv_ctx** out);
+
+/* Free the host-side context (the workspace stays the caller's). */
+void confkv_destroy(confkv_ctx* ctx);
+
+/*
+ * Ingest the prefill and reset the cache.  k, v: device fp16
+ * [L][B][Hkv][t_max][d]; sequence b uses its first prefill_len[b] tokens
+ * (prefill_len is a HOST array of B values, 0 <= prefill_len[b] <= t_max).
+ * Scales per (layer, sequence, KV head, channel) from the absmax over the
+ * prefill: s = absmax / 127 in float32 (1 if the channel is zero).  Positions
+ * >= prefill_len - W stay FP16; older positions are stored as INT8 codes
+ * clamp(rint(x / s), -127, 127) ([gist-de] Systemintegration; the pages do
+ * not describe prefill, this rule follows their per-head per-channel INT8).
+ * EMA mass starts at 0.  Returns CONFKV_ECAPACITY if prefill_len - W > cap.
+ */
+int confkv_prefill(confkv_ctx* ctx, const int32_t* prefill_len, const void* k, const void* v,
+                   int64_t t_max, void* stream);
+
+/*
+ * One decode step for all B sequences: the token at position
+ * t_b = prefill_len[b] + (steps done since prefill) ([rainbus] 方法步骤详情,
+ * Algorithm 1):
+ *   q      [L][B][Hq][d]  fp16 or bf16 (q_dtype): the decode query
+ *   k_new  [L][B][Hkv][d] fp16, v_new likewise: the new token's K/V
+ *   logits [B][V] fp32: next-token logits (temperature 1)
+ * Outputs (device):
+ *   out         [L][B][Hq][d] fp32: attention of q over the cache plus the new
+ *               token, before any eviction of this step
+ *   budget      [B][L] int32: N chosen for (sequence, layer)
+ *   confidence  [B] fp32 or NULL: c of each sequence
+ *   evicted_pos [L][B][max_evict] int32: absolute positions evicted by this
+ *               step, ascending; only the first n_evicted[l][b] entries of a
+ *               row are written
+ *   n_evicted   [L][B] int32
+ * The step computes c = w_H(1 - H/log V) + w_m sigmoid(log p1 - log p2) +
+ * w_p p1, N = n_high if c >= tau else n_low, attention with the per-token
+ * attention mass averaged over query heads, the EMA a <- lam a + (1 - lam) A,
+ * and, if the cache holds more than N entries (the new token not counted),
+ * evicts the n - N lowest s = alpha a_hat + (1 - alpha) r_hat among entries
+ * older than the newest P, compacts the INT8 region, requantises the entry
+ * that leaves the FP16 window and appends the new token.
+ * Returns CONFKV_ECAPACITY (before launching anything) if the worst case of
+ * this step could overflow cap or max_evict.
+ */
+int confkv_step(confkv_ctx* ctx, const void* q, const void* k_new, const void* v_new,
+                const float* logits, float* out, int32_t* budget, float* confidence,
+                int32_t* evicted_pos, int32_t* n_evicted, void* stream);
+
+/*
+ * confkv_step with HOST buffers (same shapes): copies the inputs to device
+ * staging buffers inside the workspace, runs the step and copies the outputs
+ * back, all on `stream`, then synchronises the stream.  Pinned host memory
+ * makes the copies asynchronous DMA.  confidence may be NULL.
+ */
+int confkv_step_host(confkv_ctx* ctx, const void* q, const void* k_new, const void* v_new,
+                     const float* logits, float* out, int32_t* budget, float* confidence,
+                     int32_t* evicted_pos, int32_t* n_evicted, void* stream);
+
+/* Cache of one (sequence b, layer l) in a plain host layout.  Caller-owned
+ * buffers sized for cap INT8 entries and W + 16 FP16 entries:
+ *   pos8[cap], ema8[cap], k8/v8[cap][Hkv][d] int8 codes,
+ *   posR[W+16], emaR[W+16], k16/v16[W+16][Hkv][d] fp16 bit patterns,
+ *   sK, sV [Hkv][d] fp32 scales.
+ * INT8 entries are listed in slot order, FP16 entries in ring-slot order. */
+typedef struct confkv_unit_host {
+  int32_t n8, nR;
+  int32_t* pos8;
+  float* ema8;
+  int8_t* k8;
+  int8_t* v8;
+  int32_t* posR;
+  float* emaR;
+  uint16_t* k16;
+  uint16_t* v16;
+  float* sK;
+  float* sV;
+} confkv_unit_host;
+
+/* Copy the cache of (b, l) to host (synchronises `stream`). */
+int confkv_export_unit(confkv_ctx* ctx, int32_t b, int32_t l, confkv_unit_host* out, void* stream);
+
+/* Overwrite the cache of (b, l) from host buffers in the export layout
+ * (synchronises `stream`).  FP16 entries go to ring slot pos mod (W + 16);
+ * two entries must not share a slot.  Used to resume from a checkpoint or to
+ * load a crafted state. */
+int confkv_import_unit(confkv_ctx* ctx, int32_t b, int32_t l, const confkv_unit_host* in,
+                       void* stream);
+
+/* Position clock: prefill_len[B] (host) and the number of steps done since
+ * prefill.  confkv_set_clock restores it with a checkpoint. */
+int confkv_get_clock(confkv_ctx* ctx, int32_t* prefill_len, int64_t* steps);
+int confkv_set_clock(confkv_ctx* ctx, const int32_t* prefill_len, int64_t steps, void* stream);
+
+typedef struct confkv_stats {
+  int64_t steps;             /* steps since prefill */
+  int64_t evicted;           /* entries evicted since prefill */
+  int64_t moved;             /* entries moved by compaction */
+  int64_t requantised;       /* entries moved from FP16 to INT8 */
+  double attn_bytes;         /* algorithmic bytes of the attention kernel, summed */
+  double step_bytes;         /* algorithmic bytes of whole steps, summed */
+  int64_t resident;          /* cache entries resident now, all units */
+  int64_t resident_bytes;    /* K/V bytes resident now at stored widths */
+  int32_t device_status;     /* raw device status bits (0 = ok) */
+} confkv_stats;
+
+/* Read the counters and the device status word (synchronises `stream`).
+ * Returns CONFKV_EDEVICE if the status word is non-zero. */
+int confkv_get_stats(confkv_ctx* ctx, confkv_stats* out, void* stream);
+
+/* Per-kernel timing with CUDA events on the launching stream.  While enabled,
+ * every confkv_step records events around its three kernels (confidence and
+ * append / attention / select-compact-requant).  confkv_profile_read
+ * synchronises and returns the summed milliseconds of each and the number of
+ * steps recorded, then clears them.  At most `max_steps` steps are kept. */
+int confkv_profile_enable(confkv_ctx* ctx, int32_t max_steps);
+int confkv_profile_disable(confkv_ctx* ctx);
+int confkv_profile_read(confkv_ctx* ctx, double* ms_prestep, double* ms_attention,
+                        double* ms_select, int32_t* steps);
+
+/* Attention launch shape chosen for the next step: CTAs per (layer, sequence,
+ * KV head) and dynamic shared memory per CTA. */
+int confkv_attention_plan(confkv_ctx* ctx, int32_t* splits, int32_t* smem_bytes);
+
+/* Byte offset of (token tau in [0,16), channel c) inside one 16-token block of
+ * the device layout: kind 0 = INT8 K, 1 = INT8 V, 2 = FP16 K, 3 = FP16 V.
+ * Host-only helper for tests of the interleave; -1 for bad arguments. */
+int32_t confkv_block_offset(int32_t kind, int32_t d, int32_t tau, int32_t c);
+
+/* Human-readable text of a status code. */
+const char* confkv_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t confkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CONFKV_H */

@@ -1,0 +1,184 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path (through the C
+ABI binding) and the CPU oracle on the same seeded inputs and compare.
+
+Tolerances: attention output <= 2e-3 max-abs, EMA <= 1e-5, confidence <= 1e-6;
+budgets, evicted positions, INT8 codes, FP16 values, scales and positions
+exact.  Two floating-point decisions may legitimately differ between the
+float64 oracle and the GPU: a budget when |c - tau| < 1e-6, and an eviction
+among candidates whose oracle score lies within 1e-5 of the k-th score.
+Those cases are flagged, checked for validity (right count, only
+candidates), and the GPU is re-synchronised to the oracle's state by
+importing it (inputs only ever flow oracle -> GPU, never the other way).
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import torch
+
+from oracle import confkv_oracle as orc
+import confidence_gated_kv_gb300 as ck
+
+OUT_TOL = 2e-3
+EMA_TOL = 1e-5
+C_TOL = 1e-6
+TAU_BAND = 1e-6
+TIE_BAND = 1e-5
+
+
+@dataclasses.dataclass
+class Flags:
+    budget: int = 0
+    ties: int = 0
+    steps: int = 0
+    evictions: int = 0
+    max_out_err: float = 0.0
+    max_ema_err: float = 0.0
+
+
+def unit_to_host(st: orc.UnitState) -> dict:
+    """Oracle state of one (sequence, layer) in the library's import layout."""
+    i8 = st.is8
+    return dict(pos8=st.pos[i8].astype(np.int32), ema8=st.a[i8].astype(np.float32),
+                k8=st.kc[i8], v8=st.vc[i8], posR=st.pos[~i8].astype(np.int32),
+                emaR=st.a[~i8].astype(np.float32), k16=st.kh[~i8], v16=st.vh[~i8],
+                sK=st.sK, sV=st.sV)
+
+
+def compare_unit(gpu: dict, st: orc.UnitState, where: str, ema_tol: float = EMA_TOL) -> float:
+    """Exported GPU unit vs oracle unit.  Returns the max EMA error."""
+    gpos = np.concatenate([gpu["pos8"], gpu["posR"]]).astype(np.int64)
+    assert np.array_equal(np.sort(gpos), np.sort(st.pos)), where + ": resident positions differ"
+    np.testing.assert_array_equal(gpu["sK"], st.sK, err_msg=where + ": K scales")
+    np.testing.assert_array_equal(gpu["sV"], st.sV, err_msg=where + ": V scales")
+    idx = {int(p): i for i, p in enumerate(st.pos)}
+    i8 = np.array([idx[int(p)] for p in gpu["pos8"]], dtype=np.int64)
+    iR = np.array([idx[int(p)] for p in gpu["posR"]], dtype=np.int64)
+    assert np.all(st.is8[i8]) and not np.any(st.is8[iR]), where + ": FP16 / INT8 membership"
+    np.testing.assert_array_equal(gpu["k8"], st.kc[i8], err_msg=where + ": K codes")
+    np.testing.assert_array_equal(gpu["v8"], st.vc[i8], err_msg=where + ": V codes")
+    np.testing.assert_array_equal(gpu["k16"], st.kh[iR], err_msg=where + ": K fp16")
+    np.testing.assert_array_equal(gpu["v16"], st.vh[iR], err_msg=where + ": V fp16")
+    err = 0.0
+    if i8.size:
+        err = max(err, float(np.abs(gpu["ema8"].astype(np.float64) - st.a[i8]).max()))
+    if iR.size:
+        err = max(err, float(np.abs(gpu["emaR"].astype(np.float64) - st.a[iR]).max()))
+    assert err <= ema_tol, "%s: EMA error %.3g" % (where, err)
+    return err
+
+
+def check_evictions(gpu_ev: np.ndarray, r: orc.UnitStepResult, where: str) -> bool:
+    """True if the GPU evicted exactly the oracle's set; False for an allowed
+    difference inside the tie band (raises otherwise)."""
+    want = np.asarray(r.evicted)
+    got = np.asarray(gpu_ev)
+    assert got.size == want.size, "%s: evicted %d, oracle %d" % (where, got.size, want.size)
+    assert np.all(np.diff(got) > 0) if got.size > 1 else True, where + ": not ascending"
+    if np.array_equal(got, want):
+        return True
+    # only candidates inside the tie band of the k-th score may differ
+    order = np.lexsort((r.cand_pos, r.scores))
+    kth = r.scores[order[r.k - 1]]
+    amb = set(r.cand_pos[np.abs(r.scores - kth) < TIE_BAND].tolist())
+    cand = set(r.cand_pos.tolist())
+    assert set(got.tolist()) <= cand, where + ": evicted a non-candidate"
+    assert set(got.tolist()) - amb == set(want.tolist()) - amb, where + ": eviction outside the tie band"
+    return False
+
+
+class Pair:
+    """CUDA cache + oracle driven by the same inputs."""
+
+    def __init__(self, w, seed: int, prefill_len=None, cap=None, max_evict=0, k=None, v=None):
+        self.w = w
+        self.seed = seed
+        self.prm = orc.Params.from_workload(w)
+        self.T0 = list(prefill_len) if prefill_len is not None else [w.T0] * w.B
+        if k is None:
+            from workload import prefill_batch
+            k, v = prefill_batch(w, seed, "cpu", T0=max(self.T0) if self.T0 else 0)
+        self.oracle = orc.Oracle(self.prm)
+        self.oracle.prefill(k, v, self.T0)
+        self.cache = ck.Cache(ck.config_from_workload(w, cap=cap, max_evict=max_evict))
+        self.cache.prefill(k.cuda(), v.cuda(), self.T0)
+        self.flags = Flags()
+
+    def resync(self):
+        for l in range(self.w.L):
+            for b in range(self.w.B):
+                self.cache.import_unit(b, l, unit_to_host(self.oracle.states[l][b]))
+
+    def compare_states(self, units=None):
+        units = units or [(b, l) for b in range(self.w.B) for l in range(self.w.L)]
+        for b, l in units:
+            e = compare_unit(self.cache.export_unit(b, l), self.oracle.states[l][b], "unit b%d l%d" % (b, l))
+            self.flags.max_ema_err = max(self.flags.max_ema_err, e)
+
+    def step(self, q, kn, vn, lg, check_state=True):
+        w = self.w
+        o = self.cache.step(q.cuda(), kn.cuda(), vn.cuda(), lg.cuda())
+        torch.cuda.synchronize()
+        res = self.oracle.step(q, kn, vn, lg)
+        self.flags.steps += 1
+        out = o["out"].cpu().numpy()
+        bud = o["budget"].cpu().numpy()
+        conf = o["confidence"].cpu().numpy()
+        nev = o["n_evicted"].cpu().numpy()
+        ev = o["evicted"].cpu().numpy()
+        diverged = False
+        for b in range(w.B):
+            assert abs(conf[b] - res.c[b]) <= C_TOL, "c of seq %d: %r vs %r" % (b, conf[b], res.c[b])
+            near = abs(res.c[b] - w.tau) < TAU_BAND
+            if not np.array_equal(bud[b], res.budget[b]):
+                assert near, "budget of seq %d differs with c = %r" % (b, res.c[b])
+                self.flags.budget += 1
+                diverged = True
+        err = float(np.abs(out - res.out).max())
+        self.flags.max_out_err = max(self.flags.max_out_err, err)
+        assert err <= OUT_TOL, "attention output error %.3g" % err
+        if not diverged:
+            for l in range(w.L):
+                for b in range(w.B):
+                    where = "step %d l%d b%d" % (self.oracle.step_idx - 1, l, b)
+                    k = int(nev[l, b])
+                    r = res.units[l][b]
+                    assert k == r.k, "%s: n_evicted %d vs %d" % (where, k, r.k)
+                    self.flags.evictions += k
+                    if k and not check_evictions(ev[l, b, :k], r, where):
+                        self.flags.ties += 1
+                        diverged = True
+        if diverged:
+            self.resync()
+        elif check_state:
+            self.compare_states()
+        st = self.cache.stats()
+        assert st["device_status"] == 0
+        return o, res
+
+
+def step_inputs(w, seed: int, r: int):
+    """Pooled step inputs r of the whole batch (CPU torch tensors)."""
+    from workload import step_unit, step_logits
+    qdt = torch.bfloat16 if w.q_dtype == "bf16" else torch.float16
+    q = torch.empty((w.L, w.B, w.Hq, w.d), dtype=qdt)
+    kn = torch.empty((w.L, w.B, w.Hkv, w.d), dtype=torch.float16)
+    vn = torch.empty_like(kn)
+    lg = torch.empty((w.B, w.V), dtype=torch.float32)
+    for b in range(w.B):
+        lg[b] = torch.from_numpy(step_logits(w, seed, r, b))
+        for l in range(w.L):
+            qq, kk, vv = step_unit(w, seed, r, b, l)
+            q[l, b] = qq
+            kn[l, b] = torch.from_numpy(kk)
+            vn[l, b] = torch.from_numpy(vv)
+    return q, kn, vn, lg
+
+
+def confident_logits(V: int, B: int, seed: int) -> torch.Tensor:
+    """Logits with one overwhelming token: c close to 1 (tight budget)."""
+    g = np.random.default_rng(seed)
+    lg = g.normal(size=(B, V)).astype(np.float32)
+    lg[np.arange(B), g.integers(0, V, B)] += 40.0
+    return torch.from_numpy(lg)

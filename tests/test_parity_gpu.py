@@ -1,0 +1,167 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle on the
+same seeded inputs, at sizes the oracle finishes in seconds that span several
+16-token blocks, ragged tails, empty prefills, budget flips, the split-K
+cluster path and both head dims."""
+import numpy as np
+import pytest
+import torch
+
+import confidence_gated_kv_gb300 as ck
+from workload import Workload, get_workload, prefill_batch
+
+from _parity import Pair, confident_logits, step_inputs
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(w, seed, steps, prefill_len=None, confident_every=0, cap=None, check_state=True):
+    p = Pair(w, seed, prefill_len=prefill_len, cap=cap)
+    p.compare_states()
+    for s in range(steps):
+        q, kn, vn, lg = step_inputs(w, seed, s)
+        if confident_every and s % confident_every == confident_every - 1:
+            lg = confident_logits(w.V, w.B, seed * 1000 + s)
+        p.step(q, kn, vn, lg, check_state=check_state)
+    return p
+
+
+def test_gqa5_d128_ragged_prefills_and_flips():
+    w = Workload(name="t_gqa", B=3, L=2, Hq=10, Hkv=2, d=128, V=3000, T0=300, steps=40,
+                 n_high=(40, 30), n_low=(120, 90), P=8, W=32, q_dtype="bf16",
+                 heavy_count=5, heavy_factor=3.0, logit_sigma=1.5, spike_hi=14.0)
+    p = _run(w, 11, 40, prefill_len=[300, 17, 0], confident_every=5)
+    assert p.flags.evictions > 0
+    assert p.flags.max_out_err <= 2e-3
+
+
+def test_mha_d64_fp16_queries():
+    w = Workload(name="t_mha", B=2, L=3, Hq=4, Hkv=4, d=64, V=5000, T0=200, steps=30,
+                 n_high=(64,) * 3, n_low=(128,) * 3, P=16, W=64, q_dtype="f16",
+                 heavy_count=3, heavy_factor=4.0)
+    p = _run(w, 12, 30, prefill_len=[200, 150], confident_every=4)
+    assert p.flags.evictions > 0
+
+
+def test_gqa8_pyramidal_budgets():
+    w = Workload(name="t_g8", B=2, L=3, Hq=16, Hkv=2, d=128, V=2000, T0=160, steps=20,
+                 n_high=(48, 40, 32), n_low=(96, 80, 64), P=12, W=24, q_dtype="f16")
+    p = _run(w, 13, 20, confident_every=3)
+    assert p.flags.evictions > 0
+
+
+def test_split_k_cluster_path_and_large_first_eviction():
+    w = Workload(name="t_split", B=1, L=1, Hq=8, Hkv=2, d=128, V=4000, T0=2000, steps=6,
+                 n_high=(300,), n_low=(600,), P=16, W=64, q_dtype="bf16", heavy_count=10,
+                 heavy_factor=3.0)
+    p = Pair(w, 14)
+    splits, smem = p.cache.attention_plan()
+    assert splits > 1
+    for s in range(6):
+        q, kn, vn, lg = step_inputs(w, 14, s)
+        if s == 3:
+            lg = confident_logits(w.V, w.B, 99)
+        p.step(q, kn, vn, lg)
+    assert p.flags.evictions >= 2000 - 600
+
+
+def test_no_eviction_limit_is_plain_attention():
+    # budgets above every cache length: nothing is evicted, nothing moves
+    w = Workload(name="t_noop", B=2, L=2, Hq=6, Hkv=3, d=64, V=1000, T0=40, steps=12,
+                 n_high=(10 ** 5,) * 2, n_low=(10 ** 5,) * 2, P=4, W=16, q_dtype="f16", cap=80)
+    p = _run(w, 15, 12)
+    assert p.flags.evictions == 0
+    st = p.cache.stats()
+    assert st["evicted"] == 0 and st["moved"] == 0
+    assert st["requantised"] == 2 * 2 * 12
+
+
+def test_gpt2_small_batch1_full_trajectory():
+    # GPT-2-small geometry, 600-token prefill, all 64 decode steps free-running
+    w = get_workload("gpt2_b1")
+    p = _run(w, 1001, w.steps, check_state=False)
+    p.compare_states()
+    assert p.flags.steps == 64
+    assert p.flags.max_out_err <= 2e-3
+
+
+def test_gpt2_small_batch8_pyramid_prefix():
+    w = get_workload("gpt2_b8_pyramid")
+    p = _run(w, 1002, 24, confident_every=6, check_state=False)
+    p.compare_states()
+
+
+def test_host_buffer_step_matches_device_step():
+    w = Workload(name="t_host", B=2, L=2, Hq=8, Hkv=2, d=128, V=3000, T0=100, steps=5,
+                 n_high=(40, 40), n_low=(64, 64), P=8, W=16, q_dtype="bf16")
+    k, v = prefill_batch(w, 16, "cpu")
+    a = ck.Cache(ck.config_from_workload(w))
+    b = ck.Cache(ck.config_from_workload(w))
+    a.prefill(k.cuda(), v.cuda(), [w.T0] * w.B)
+    b.prefill(k.cuda(), v.cuda(), [w.T0] * w.B)
+    hout = b.host_outputs()
+    for s in range(5):
+        q, kn, vn, lg = step_inputs(w, 16, s)
+        o = a.step(q.cuda(), kn.cuda(), vn.cuda(), lg.cuda())
+        b.step_host(q.pin_memory(), kn.pin_memory(), vn.pin_memory(), lg.pin_memory(), hout)
+        torch.cuda.synchronize()
+        assert torch.equal(o["out"].cpu(), hout["out"])
+        assert torch.equal(o["budget"].cpu(), hout["budget"])
+        assert torch.equal(o["n_evicted"].cpu(), hout["n_evicted"])
+        n = o["n_evicted"].cpu()
+        for l in range(w.L):
+            for bb in range(w.B):
+                kk = int(n[l, bb])
+                assert torch.equal(o["evicted"][l, bb, :kk].cpu(), hout["evicted"][l, bb, :kk])
+
+
+def test_export_import_round_trip_resumes_identically():
+    w = Workload(name="t_ckpt", B=2, L=2, Hq=8, Hkv=4, d=64, V=2000, T0=90, steps=8,
+                 n_high=(30, 30), n_low=(60, 60), P=6, W=16, q_dtype="f16")
+    k, v = prefill_batch(w, 17, "cpu")
+    a = ck.Cache(ck.config_from_workload(w))
+    a.prefill(k.cuda(), v.cuda(), [w.T0] * w.B)
+    for s in range(4):
+        a.step(*(t.cuda() for t in step_inputs(w, 17, s)))
+    b = ck.Cache(ck.config_from_workload(w))
+    for l in range(w.L):
+        for bb in range(w.B):
+            b.import_unit(bb, l, a.export_unit(bb, l))
+    pl, steps = a.get_clock()
+    b.set_clock(pl, steps)
+    for s in range(4, 8):
+        ins = [t.cuda() for t in step_inputs(w, 17, s)]
+        oa = a.step(*ins)
+        ob = b.step(*ins)
+        torch.cuda.synchronize()
+        assert torch.equal(oa["out"], ob["out"])
+        assert torch.equal(oa["n_evicted"], ob["n_evicted"])
+
+
+def test_capacity_is_checked_before_launch():
+    w = Workload(name="t_cap", B=1, L=1, Hq=4, Hkv=4, d=64, V=1000, T0=40, steps=4,
+                 n_high=(10 ** 5,), n_low=(10 ** 5,), P=4, W=8, q_dtype="f16", cap=48)
+    k, v = prefill_batch(w, 18, "cpu")
+    c = ck.Cache(ck.config_from_workload(w))
+    c.prefill(k.cuda(), v.cuda(), [40])
+    for s in range(16):
+        try:
+            c.step(*(t.cuda() for t in step_inputs(w, 18, s)))
+        except ck.ConfkvError as e:
+            assert e.status == -2
+            break
+    else:
+        pytest.fail("capacity overflow not reported")
+    assert c.stats()["device_status"] == 0
+    # a prefill longer than cap + W is rejected too
+    k2 = torch.zeros((1, 1, 4, 80, 64), dtype=torch.float16, device="cuda")
+    with pytest.raises(ck.ConfkvError):
+        c.prefill(k2, k2, [80])
+
+
+def test_step_before_prefill_is_an_order_error():
+    w = Workload(name="t_ord", B=1, L=1, Hq=4, Hkv=4, d=64, V=1000, T0=10, steps=1,
+                 n_high=(16,), n_low=(16,), P=4, W=8)
+    c = ck.Cache(ck.config_from_workload(w))
+    with pytest.raises(ck.ConfkvError) as e:
+        c.step(*(t.cuda() for t in step_inputs(w, 19, 0)))
+    assert e.value.status == -7

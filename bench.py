@@ -222,12 +222,16 @@ def run_ours(args):
     from workload import get_workload, prefill_batch_fast, step_pool_fast
 
     w = get_workload(args.workload)
+    if args.batch:
+        w = w.replace(B=args.batch)
     seed = args.seed + 7919 * rank
     cfg = ck.config_from_workload(w)
     cache = ck.Cache(cfg, device=dev)
     k, v = prefill_batch_fast(w, seed, dev)
     cache.prefill(k, v, [w.T0] * w.B)
+    torch.cuda.synchronize()
     del k, v
+    torch.cuda.empty_cache()
     R = args.pool
     q, kn, vn, lg = step_pool_fast(w, seed, R, dev)
     outs = cache.new_outputs()
@@ -344,9 +348,10 @@ def run_ours(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=8)
     ap.add_argument("--workload", default="qwen32b")
+    ap.add_argument("--batch", type=int, default=0, help="override the workload's batch (small captures)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=4003)
     ap.add_argument("--pool", type=int, default=16)

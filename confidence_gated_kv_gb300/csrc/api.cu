@@ -91,8 +91,8 @@ size_t layout(const Shape& s, char* base, Dev* d, Staging* st) {
   const size_t units = (size_t)s.L * s.B * s.Hkv;
   const size_t lbs = (size_t)s.L * s.B;
   Dev dd{};
-  dd.k8 = cv.take<int8_t>(units * s.cap * s.D);
-  dd.v8 = cv.take<int8_t>(units * s.cap * s.D);
+  dd.k8 = cv.take<uint8_t>(units * s.cap * s.D);
+  dd.v8 = cv.take<uint8_t>(units * s.cap * s.D);
   dd.k16 = cv.take<__half>(units * s.WR * s.D);
   dd.v16 = cv.take<__half>(units * s.WR * s.D);
   dd.sK = cv.take<float>(units * s.D);
@@ -109,6 +109,8 @@ size_t layout(const Shape& s, char* base, Dev* d, Staging* st) {
   dd.stats = cv.take<DevStats>(1);
   dd.status = cv.take<int32_t>(1);
   dd.absmax = cv.take<uint32_t>(2 * units * s.D);
+  dd.score_ctas = attention_persistent_ctas();
+  dd.scores = cv.take<float>((size_t)dd.score_ctas * 2 * s.G * s.S);
   Staging sg{};
   sg.q = cv.take<uint16_t>(lbs * s.Hq * s.D);
   sg.k_new = cv.take<uint16_t>(units * s.D);
@@ -332,7 +334,7 @@ int confkv_step_host(confkv_ctx* ctx, const void* q, const void* k_new, const vo
 
 // ------------------------------------------------------------------ export / import
 
-static int copy_unit_raw(confkv_ctx* ctx, int b, int l, std::vector<int8_t>& k8, std::vector<int8_t>& v8,
+static int copy_unit_raw(confkv_ctx* ctx, int b, int l, std::vector<uint8_t>& k8, std::vector<uint8_t>& v8,
                          std::vector<uint16_t>& k16, std::vector<uint16_t>& v16, std::vector<int32_t>& pos,
                          std::vector<float>& ema, std::vector<float>& sK, std::vector<float>& sV, int32_t& n8,
                          cudaStream_t st) {
@@ -367,7 +369,7 @@ int confkv_export_unit(confkv_ctx* ctx, int32_t b, int32_t l, confkv_unit_host* 
     return CONFKV_EINVAL;
   const Shape& s = ctx->s;
   const int D = s.D, Hkv = s.Hkv;
-  std::vector<int8_t> k8, v8;
+  std::vector<uint8_t> k8, v8;
   std::vector<uint16_t> k16, v16;
   std::vector<int32_t> pos;
   std::vector<float> ema, sK, sV;
@@ -381,8 +383,8 @@ int confkv_export_unit(confkv_ctx* ctx, int32_t b, int32_t l, confkv_unit_host* 
     for (int h = 0; h < Hkv; ++h) {
       const size_t blk = ((size_t)h * s.cap + (i & ~15)) * D;
       for (int c = 0; c < D; ++c) {
-        o->k8[((size_t)i * Hkv + h) * D + c] = k8[blk + k8_offset(D, i & 15, c)];
-        o->v8[((size_t)i * Hkv + h) * D + c] = v8[blk + v8_offset(D, i & 15, c)];
+        o->k8[((size_t)i * Hkv + h) * D + c] = (int8_t)((int)k8[blk + k8_offset(D, i & 15, c)] - kCodeBias);
+        o->v8[((size_t)i * Hkv + h) * D + c] = (int8_t)((int)v8[blk + v8_offset(D, i & 15, c)] - kCodeBias);
       }
     }
   }
@@ -418,7 +420,7 @@ int confkv_import_unit(confkv_ctx* ctx, int32_t b, int32_t l, const confkv_unit_
   if ((in->n8 && (!in->pos8 || !in->ema8 || !in->k8 || !in->v8)) ||
       (in->nR && (!in->posR || !in->emaR || !in->k16 || !in->v16)) || !in->sK || !in->sV)
     return CONFKV_EINVAL;
-  std::vector<int8_t> k8((size_t)Hkv * s.cap * D, 0), v8(k8.size(), 0);
+  std::vector<uint8_t> k8((size_t)Hkv * s.cap * D, kCodeBias), v8(k8.size(), kCodeBias);
   std::vector<uint16_t> k16((size_t)Hkv * s.WR * D, 0), v16(k16.size(), 0);
   std::vector<int32_t> pos(s.S, -1);
   std::vector<float> ema(s.S, 0.f);
@@ -429,8 +431,10 @@ int confkv_import_unit(confkv_ctx* ctx, int32_t b, int32_t l, const confkv_unit_
     for (int h = 0; h < Hkv; ++h) {
       const size_t blk = ((size_t)h * s.cap + (i & ~15)) * D;
       for (int c = 0; c < D; ++c) {
-        k8[blk + k8_offset(D, i & 15, c)] = in->k8[((size_t)i * Hkv + h) * D + c];
-        v8[blk + v8_offset(D, i & 15, c)] = in->v8[((size_t)i * Hkv + h) * D + c];
+        const int ck = in->k8[((size_t)i * Hkv + h) * D + c], cv = in->v8[((size_t)i * Hkv + h) * D + c];
+        if (ck < -127 || cv < -127) return CONFKV_EINVAL;   // codes are symmetric
+        k8[blk + k8_offset(D, i & 15, c)] = (uint8_t)(ck + kCodeBias);
+        v8[blk + v8_offset(D, i & 15, c)] = (uint8_t)(cv + kCodeBias);
       }
     }
   }

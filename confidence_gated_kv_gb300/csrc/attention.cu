@@ -9,11 +9,19 @@
 // mass is the softmax probability averaged over the query heads.
 //
 // Work decomposition: one unit = (layer, sequence, KV head); its G = Hq/Hkv
-// query heads share the unit's K/V.  A unit's token blocks (INT8 blocks first,
-// then the FP16 ring) are split over `splits` CTAs that form one thread-block
-// cluster; inside a CTA each warp takes every NW-th block.
+// query heads share the unit's K/V.  A unit's 16-token blocks (INT8 blocks
+// first, then the FP16 ring) are split over `splits` CTAs that form one
+// thread-block cluster.
 //
-// Per 16-token block a warp issues two tensor-core products with
+// Data movement: a producer warp streams the CTA's blocks into a ring of
+// shared-memory stages with cp.async.bulk (1-D TMA) completing on mbarriers;
+// an INT8 stage is 4 blocks (K span + V span, contiguous in HBM), an FP16
+// stage 2 blocks, both 128*D bytes.  Four consumer warps take one block of a
+// stage each and release the stage on an "empty" mbarrier.  Every wait is
+// bounded: on time-out the kernel sets a status bit, drains its own copies
+// and finishes without hanging.
+//
+// Per 16-token block a consumer warp issues two tensor-core products with
 // mma.sync.m16n8k16 (fp16 in, fp32 accumulate):
 //   QK^T: A = the G query rows, as fp16 "hi" parts in rows 0..G-1 and the
 //         fp16 remainders q - hi in rows 8..8+G-1 (near-fp32 accuracy for
@@ -38,10 +46,57 @@ namespace cg = cooperative_groups;
 
 namespace confkv {
 
-constexpr int kAttnWarps = 4;
-constexpr int kAttnThreads = kAttnWarps * 32;
-constexpr float kQPre = 256.0f;         // q pre-scale before the hi/lo split
+constexpr int kConsumerWarps = 4;
+constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxStages = 8;
+constexpr long long kSpinLimit = 1LL << 22;   // mbarrier polls per wait
+constexpr float kQPre = 256.0f;               // q pre-scale before the hi/lo split
 constexpr float kQPreInv = 1.0f / 256.0f;
+
+// ---------------------------------------------------------------- PTX helpers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false after kSpinLimit polls.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (long long i = 0; i < kSpinLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
 
 __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
@@ -52,18 +107,33 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Four signed int8 (bytes 0..3 of w) -> two half2 {byte0, byte1}, {byte2,
-// byte3}, exactly: byte ^ 0x80 = code + 128 = u; the fp16 with bits
-// 0x6400 | u is 1024 + u; subtracting 1152 leaves the code.
-__device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t& b0, uint32_t& b1) {
-  const uint32_t x = w ^ 0x80808080u;
-  uint32_t lo = __byte_perm(x, 0x64646464u, 0x5140);
-  uint32_t hi = __byte_perm(x, 0x64646464u, 0x5342);
+// Stored INT8 bytes are code + 128 = u.  The fp16 with bits 0x6400 | u is
+// exactly 1024 + u = 1152 + code, so two byte permutes turn four stored bytes
+// into two half2 operands {byte0, byte1}, {byte2, byte3}.
+//  - K operand: used as is; the constant 1152 contributes 1152 * sum_c q'_c to
+//    every score of a query row, which is subtracted once per block in fp32
+//    (the QK accumulator restarts at zero every block).
+//  - V operand: the PV accumulator runs over all blocks, so 1152 is removed
+//    exactly with one packed fp16 subtract, leaving the code.
+__device__ __forceinline__ void u8x4_to_h2x2_biased(uint32_t w, uint32_t& b0, uint32_t& b1) {
+  b0 = __byte_perm(w, 0x64646464u, 0x5140);
+  b1 = __byte_perm(w, 0x64646464u, 0x5342);
+}
+__device__ __forceinline__ void u8x4_to_h2x2_exact(uint32_t w, uint32_t& b0, uint32_t& b1) {
+  uint32_t lo = __byte_perm(w, 0x64646464u, 0x5140);
+  uint32_t hi = __byte_perm(w, 0x64646464u, 0x5342);
   const __half2 bias = __float2half2_rn(1152.0f);
   __half2 hl = __hsub2(*reinterpret_cast<__half2*>(&lo), bias);
   __half2 hh = __hsub2(*reinterpret_cast<__half2*>(&hi), bias);
   b0 = *reinterpret_cast<uint32_t*>(&hl);
   b1 = *reinterpret_cast<uint32_t*>(&hh);
+}
+
+// 2^x with the hardware approximation (relative error about 2^-22).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ uint32_t pack_h2(__half a, __half b) {
@@ -74,6 +144,15 @@ __device__ __forceinline__ uint32_t pack_h2(__half a, __half b) {
 __device__ __forceinline__ void split_hi_lo(float x, __half& hi, __half& lo) {
   hi = __float2half_rn(x);
   lo = __float2half_rn(x - __half2float(hi));
+}
+
+// Two floats -> packed hi = fp16(x), lo = fp16(x - hi) pairs.
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __float22half2_rn(make_float2(x0, x1));
+  const float2 hf = __half22float2(h);
+  const __half2 r = __float22half2_rn(make_float2(x0 - hf.x, x1 - hf.y));
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&r);
 }
 
 __device__ __forceinline__ float load_q(const void* q, size_t idx, int bf16) {
@@ -87,10 +166,12 @@ __device__ __forceinline__ uint32_t comp(const uint4& v, int i) {
 
 // A fragments of the G query rows for all D/16 k-steps.  Row g (< G) holds
 // hi(q'_g), row g + 8 holds lo(q'_g); q'_g[c] = q_g[c] * scale[c] * qs.
+// Returns 1152 * sum_c (hi + lo) of the lane's row (for the K operand offset).
 template <int D>
-__device__ __forceinline__ void make_q_frag(uint32_t (&aq)[D / 16][4], const void* q, size_t qoff,
-                                            int bf16, const float* kscale, float qs, int G,
-                                            int g, int t) {
+__device__ __forceinline__ float make_q_frag(uint32_t (&aq)[D / 16][4], const void* q, size_t qoff,
+                                             int bf16, const float* kscale, float qs, int G,
+                                             int g, int t) {
+  float sum = 0.f;
 #pragma unroll
   for (int kk = 0; kk < D / 16; ++kk) {
     float x[4] = {0.f, 0.f, 0.f, 0.f};
@@ -105,31 +186,261 @@ __device__ __forceinline__ void make_q_frag(uint32_t (&aq)[D / 16][4], const voi
     }
     __half h[4], lo[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) split_hi_lo(x[e], h[e], lo[e]);
+    for (int e = 0; e < 4; ++e) {
+      split_hi_lo(x[e], h[e], lo[e]);
+      sum += __half2float(h[e]) + __half2float(lo[e]);
+    }
     aq[kk][0] = pack_h2(h[0], h[1]);    // row g,   k = 2t, 2t+1
     aq[kk][1] = pack_h2(lo[0], lo[1]);  // row g+8, k = 2t, 2t+1
     aq[kk][2] = pack_h2(h[2], h[3]);    // row g,   k = 2t+8, 2t+9
     aq[kk][3] = pack_h2(lo[2], lo[3]);  // row g+8, k = 2t+8, 2t+9
   }
+  sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+  sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+  return 1152.0f * sum;
 }
 
+// Online-softmax update for one 16-token block: scores sc4[nt][j] belong to
+// tokens 8*nt + 2t + j of row g.  Writes the raw scores to shared memory and
+// returns the P fragment (hi rows g, lo rows g+8).  The reference maximum
+// m_run only moves when the block maximum exceeds it by more than 8 (log2
+// units), so most blocks skip rescaling the accumulator; p = 2^(s - m_run)
+// then stays below 2^8, well inside fp16.
+template <int D>
+__device__ __forceinline__ void softmax_block(float (&sc4)[2][2], const bool (&valid)[2][2],
+                                              int G, int g, float& m_run, float& l_run,
+                                              float (&acc)[D / 8][4], float* sc_dst,
+                                              uint32_t (&pa)[4], float* sc_regs) {
+  float mloc = -INFINITY;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      if (!valid[nt][j] || g >= G) sc4[nt][j] = -INFINITY;
+      mloc = fmaxf(mloc, sc4[nt][j]);
+    }
+  mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
+  mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
+  const bool move = mloc > m_run + 8.0f;     // true for the first finite block too
+  if (__any_sync(0xffffffffu, move)) {
+    const float corr = move ? (m_run == -INFINITY ? 0.f : ex2(m_run - mloc)) : 1.0f;
+    if (move) m_run = mloc;
+    l_run *= corr;
+#pragma unroll
+    for (int j = 0; j < D / 8; ++j) {
+      acc[j][0] *= corr; acc[j][1] *= corr; acc[j][2] *= corr; acc[j][3] *= corr;
+    }
+  }
+  float p[2][2];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      p[nt][j] = (sc4[nt][j] == -INFINITY) ? 0.f : ex2(sc4[nt][j] - m_run);
+      l_run += p[nt][j];
+    }
+  if (sc_regs) {
+    sc_regs[0] = sc4[0][0]; sc_regs[1] = sc4[0][1]; sc_regs[2] = sc4[1][0]; sc_regs[3] = sc4[1][1];
+  } else if (g < G) {
+    *reinterpret_cast<float2*>(sc_dst) = make_float2(sc4[0][0], sc4[0][1]);
+    *reinterpret_cast<float2*>(sc_dst + 8) = make_float2(sc4[1][0], sc4[1][1]);
+  }
+  split2(p[0][0], p[0][1], pa[0], pa[1]);   // rows g / g+8, tokens 2t, 2t+1
+  split2(p[1][0], p[1][1], pa[2], pa[3]);   // rows g / g+8, tokens 8+2t, 9+2t
+}
+
+// Stage schedule of one CTA: INT8 blocks [a0, a1) in groups of 4, then ring
+// blocks [r0, r1) in groups of 2.
+struct Sched {
+  int a0, a1, r0, r1, n8st, nst;
+  __device__ void init(int blk0, int blk1, int nb8) {
+    a0 = blk0;
+    a1 = max(blk0, min(blk1, nb8));
+    r0 = max(blk0, nb8) - nb8;
+    r1 = max(blk1, nb8) - nb8;
+    n8st = (a1 - a0 + 3) / 4;
+    nst = n8st + (r1 - r0 + 1) / 2;
+  }
+  __device__ void first_last(int i, bool& ring, int& first, int& nb) const {
+    if (i < n8st) {
+      ring = false;
+      first = a0 + 4 * i;
+      nb = min(4, a1 - first);
+    } else {
+      ring = true;
+      first = r0 + 2 * (i - n8st);
+      nb = min(2, r1 - first);
+    }
+  }
+};
+
+// Per-warp attention state of one unit.
+template <int D>
+struct WarpState {
+  uint32_t aq[D / 16][4];   // query A fragments (INT8 version, then FP16 version)
+  float acc[D / 8][4];      // PV accumulators: rows g (hi P) and g + 8 (lo P)
+  float m_run, l_run;       // reference maximum (log2 units) and lane-partial sum
+  float qoffset;            // 1152 * sum(q') of the row (INT8 K operand offset)
+  bool in_ring;
+};
+
+template <int D>
+__device__ __forceinline__ void ws_begin(WarpState<D>& w, const void* q, size_t qoff, int bf16,
+                                         const float* sKu, float qs, int G, int g, int t) {
+  w.qoffset = make_q_frag<D>(w.aq, q, qoff, bf16, sKu, qs, G, g, t);
+#pragma unroll
+  for (int j = 0; j < D / 8; ++j) w.acc[j][0] = w.acc[j][1] = w.acc[j][2] = w.acc[j][3] = 0.f;
+  w.m_run = -INFINITY;
+  w.l_run = 0.f;
+  w.in_ring = false;
+}
+
+// Multiply what the INT8 codes accumulated by the per-channel V scale.
+template <int D>
+__device__ __forceinline__ void ws_scale_v(WarpState<D>& w, const float* sVu, int t) {
+#pragma unroll
+  for (int j = 0; j < D / 8; ++j) {
+    const float2 sv = *reinterpret_cast<const float2*>(sVu + j * 8 + 2 * t);
+    w.acc[j][0] *= sv.x; w.acc[j][1] *= sv.y; w.acc[j][2] *= sv.x; w.acc[j][3] *= sv.y;
+  }
+}
+
+// INT8 -> FP16 transition: unscaled q fragments, V scale applied to the
+// accumulator.
+template <int D>
+__device__ __forceinline__ void ws_to_ring(WarpState<D>& w, const void* q, size_t qoff, int bf16,
+                                           float qs, const float* sVu, int G, int g, int t) {
+  make_q_frag<D>(w.aq, q, qoff, bf16, nullptr, qs, G, g, t);
+  w.qoffset = 0.f;
+  ws_scale_v<D>(w, sVu, t);
+  w.in_ring = true;
+}
+
+// One INT8 block at shared-memory addresses kb / vb (16*D bytes each).
+template <int D>
+__device__ __forceinline__ void int8_block(WarpState<D>& w, uint32_t kb, uint32_t vb, int blk,
+                                           int n8, int G, int g, int t, int lane, float* sc_dst,
+                                           float* sc_regs = nullptr) {
+  constexpr int NC = D / 32;
+  uint4 kw[NC], vw[NC];
+#pragma unroll
+  for (int r = 0; r < NC; ++r) kw[r] = lds128(kb + r * 512 + lane * 16);
+#pragma unroll
+  for (int r = 0; r < NC; ++r) vw[r] = lds128(vb + r * 512 + lane * 16);
+  float sc4[2][2];
+  bool valid[2][2];
+  const bool full = blk * 16 + 16 <= n8;
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      uint32_t b0, b1;
+      u8x4_to_h2x2_biased(comp(kw[nt * (NC / 2) + (kk >> 2)], kk & 3), b0, b1);
+      mma16816(c, w.aq[kk], b0, b1);
+    }
+    sc4[nt][0] = ((c[0] + c[2]) - w.qoffset) * kQPreInv;
+    sc4[nt][1] = ((c[1] + c[3]) - w.qoffset) * kQPreInv;
+    const int tok = blk * 16 + nt * 8 + 2 * t;
+    valid[nt][0] = full || tok < n8;
+    valid[nt][1] = full || tok + 1 < n8;
+  }
+  uint32_t pa[4];
+  softmax_block<D>(sc4, valid, G, g, w.m_run, w.l_run, w.acc, sc_dst, pa, sc_regs);
+#pragma unroll
+  for (int j = 0; j < D / 8; ++j) {
+    uint32_t b0, b1;
+    u8x4_to_h2x2_exact(comp(vw[j >> 2], j & 3), b0, b1);
+    mma16816(w.acc[j], pa, b0, b1);
+  }
+}
+
+// One FP16 ring block at kb / vb (32*D bytes each); posb = the block's 16
+// slot positions (-1 = empty).
+template <int D>
+__device__ __forceinline__ void ring_block(WarpState<D>& w, uint32_t kb, uint32_t vb,
+                                           const int32_t* posb, int G, int g, int t, int lane,
+                                           float* sc_dst, float* sc_regs = nullptr) {
+  const int2 pv0 = *reinterpret_cast<const int2*>(posb + 2 * t);
+  const int2 pv1 = *reinterpret_cast<const int2*>(posb + 8 + 2 * t);
+  bool valid[2][2];
+  valid[0][0] = pv0.x >= 0; valid[0][1] = pv0.y >= 0;
+  valid[1][0] = pv1.x >= 0; valid[1][1] = pv1.y >= 0;
+  float sc4[2][2];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint4 w4 = lds128(kb + (nt * (D / 32) + (kk >> 1)) * 512 + lane * 16);
+      mma16816(c, w.aq[kk], comp(w4, (kk & 1) * 2), comp(w4, (kk & 1) * 2 + 1));
+    }
+    sc4[nt][0] = (c[0] + c[2]) * kQPreInv;
+    sc4[nt][1] = (c[1] + c[3]) * kQPreInv;
+  }
+  uint32_t pa[4];
+  softmax_block<D>(sc4, valid, G, g, w.m_run, w.l_run, w.acc, sc_dst, pa, sc_regs);
+#pragma unroll
+  for (int r = 0; r < D / 16; ++r) {
+    const uint4 w4 = lds128(vb + r * 512 + lane * 16);
+    mma16816(w.acc[2 * r], pa, w4.x, w4.y);
+    mma16816(w.acc[2 * r + 1], pa, w4.z, w4.w);
+  }
+}
+
+// End of a warp's blocks: V scale if it never reached the ring, the row sum
+// over the row's four lanes, and (m, l, o) to shared memory.
+template <int D>
+__device__ __forceinline__ void ws_store(WarpState<D>& w, const float* sVu, int G, int g, int t,
+                                         float* wm, float* wl, float* wo) {
+  if (!w.in_ring) ws_scale_v<D>(w, sVu, t);
+  float l = w.l_run;
+  l += __shfl_xor_sync(0xffffffffu, l, 1);
+  l += __shfl_xor_sync(0xffffffffu, l, 2);
+  if (g < G) {
+    float* o = wo + g * D;
+#pragma unroll
+    for (int j = 0; j < D / 8; ++j)
+      *reinterpret_cast<float2*>(o + j * 8 + 2 * t) =
+          make_float2(w.acc[j][0] + w.acc[j][2], w.acc[j][1] + w.acc[j][3]);
+    if (t == 0) {
+      wm[g] = w.m_run;
+      wl[g] = l;
+    }
+  }
+}
+
+__device__ __forceinline__ void named_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ===========================================================================
+// Split kernel: the blocks of one unit spread over a cluster of `splits`
+// CTAs (long caches or few units); merged through distributed shared memory.
+// ===========================================================================
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads) attention_kernel(Shape s, Dev d,
                                                                  const void* __restrict__ q,
                                                                  float* __restrict__ out,
-                                                                 int splits, int chunk_blocks) {
-  extern __shared__ __align__(16) float smem[];
+                                                                 int splits, int chunk_blocks,
+                                                                 int stages) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  constexpr int kStageBytes = 128 * D;       // 4 INT8 blocks or 2 FP16 blocks (K + V)
+  constexpr int kHalf = kStageBytes / 2;     // K span | V span
   const int G = s.G;
   const int chunk_tok = chunk_blocks * 16;
-  float* sc = smem;                                   // [G][chunk_tok] raw scores (log2 units)
+  unsigned char* sbuf = smem_raw;                                   // [stages][kStageBytes]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw + stages * kStageBytes);  // full, empty
+  float* sc = reinterpret_cast<float*>(bars + 2 * kMaxStages);      // [G][chunk_tok]
   float* wm = sc + G * chunk_tok;                     // [NW][G]
-  float* wl = wm + kAttnWarps * G;                    // [NW][G]
-  float* wo = wl + kAttnWarps * G;                    // [NW][G][D]
-  float* cm = wo + kAttnWarps * G * D;                // [G]    CTA max     (read by peers)
+  float* wl = wm + kConsumerWarps * G;                // [NW][G]
+  float* wo = wl + kConsumerWarps * G;                // [NW][G][D]
+  float* cm = wo + kConsumerWarps * G * D;            // [G]    CTA max     (read by peers)
   float* cl = cm + kMaxG;                             // [G]    CTA sum     (read by peers)
   float* co = cl + kMaxG;                             // [G][D] CTA output  (read by peers)
   float* gM = co + G * D;                             // [G]
   float* gL = gM + kMaxG;                             // [G]
+  int& s_abort = *reinterpret_cast<int*>(gL + kMaxG);  // set when a bounded wait gave up
 
   cg::cluster_group cluster = cg::this_cluster();
   const int u = blockIdx.x / splits;
@@ -142,234 +453,115 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(Shape s, Dev d,
   const int nb8 = (n8 + 15) >> 4;
   const int nbR = s.WR >> 4;
   const int nbT = nb8 + nbR;
-  const int blk0 = rank * chunk_blocks;
+  const int blk0 = min(nbT, rank * chunk_blocks);
   const int blk1 = min(nbT, blk0 + chunk_blocks);
+  Sched sch;
+  sch.init(blk0, blk1, nb8);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const size_t qoff = (lb * s.Hq + (size_t)h * G) * D;
-  const float qs = kQPre * 1.4426950408889634f * rsqrtf((float)D);
   const float* sKu = d.sK + (size_t)u * D;
   const float* sVu = d.sV + (size_t)u * D;
-  const int8_t* k8u = d.k8 + (size_t)u * s.cap * D;
-  const int8_t* v8u = d.v8 + (size_t)u * s.cap * D;
+  const uint8_t* k8u = d.k8 + (size_t)u * s.cap * D;
+  const uint8_t* v8u = d.v8 + (size_t)u * s.cap * D;
   const char* k16u = reinterpret_cast<const char*>(d.k16) + (size_t)u * s.WR * D * 2;
   const char* v16u = reinterpret_cast<const char*>(d.v16) + (size_t)u * s.WR * D * 2;
   const int32_t* posR = d.pos + lb * s.S + s.cap;
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+  auto empty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(kMaxStages + i); };
 
-  uint32_t aq[D / 16][4];
-  make_q_frag<D>(aq, q, qoff, s.qbf16, sKu, qs, G, g, t);
-  float acc[D / 8][4];
-#pragma unroll
-  for (int j = 0; j < D / 8; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-  float m_run = -INFINITY, l_run = 0.f;
-  bool in_ring = false;
-
-  for (int blk = blk0 + warp; blk < blk1; blk += kAttnWarps) {
-    const bool ring = blk >= nb8;
-    if (ring && !in_ring) {
-      // INT8 -> FP16 transition: unscaled q, and apply the V scale to what
-      // has been accumulated from codes so far.
-      make_q_frag<D>(aq, q, qoff, s.qbf16, nullptr, qs, G, g, t);
-#pragma unroll
-      for (int j = 0; j < D / 8; ++j) {
-        const float2 sv = *reinterpret_cast<const float2*>(sVu + j * 8 + 2 * t);
-        acc[j][0] *= sv.x; acc[j][1] *= sv.y; acc[j][2] *= sv.x; acc[j][3] *= sv.y;
-      }
-      in_ring = true;
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int i = 0; i < stages; ++i) {
+      mbar_init(full_bar(i), 1);
+      mbar_init(empty_bar(i), kConsumerWarps);
     }
-    float sc4[2][2];
-    bool valid[2][2];
-    if (!ring) {
-      // ------------------------------------------------ INT8 block
-      constexpr int NC = D / 32;
-      const uint4* kb = reinterpret_cast<const uint4*>(k8u + (size_t)blk * 16 * D);
-      const uint4* vb = reinterpret_cast<const uint4*>(v8u + (size_t)blk * 16 * D);
-      uint4 kw[NC], vw[NC];
-#pragma unroll
-      for (int r = 0; r < NC; ++r) kw[r] = __ldg(kb + r * 32 + lane);
-#pragma unroll
-      for (int r = 0; r < NC; ++r) vw[r] = __ldg(vb + r * 32 + lane);
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          uint32_t b0, b1;
-          i8x4_to_h2x2(comp(kw[nt * (NC / 2) + (kk >> 2)], kk & 3), b0, b1);
-          mma16816(c, aq[kk], b0, b1);
-        }
-        sc4[nt][0] = (c[0] + c[2]) * kQPreInv;
-        sc4[nt][1] = (c[1] + c[3]) * kQPreInv;
-        const int tok = blk * 16 + nt * 8 + 2 * t;
-        valid[nt][0] = tok < n8;
-        valid[nt][1] = tok + 1 < n8;
-      }
-      // softmax + PV below uses vw
-      float p[2][2];
-      {
-        float mloc = -INFINITY;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            if (!valid[nt][j] || g >= G) sc4[nt][j] = -INFINITY;
-            mloc = fmaxf(mloc, sc4[nt][j]);
-          }
-        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
-        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
-        const float m_new = fmaxf(m_run, mloc);
-        const float corr = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_new);
-        float ps = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            p[nt][j] = (sc4[nt][j] == -INFINITY) ? 0.f : exp2f(sc4[nt][j] - m_new);
-            ps += p[nt][j];
-          }
-        l_run = l_run * corr + ps;
-        m_run = m_new;
-#pragma unroll
-        for (int j = 0; j < D / 8; ++j) {
-          acc[j][0] *= corr; acc[j][1] *= corr; acc[j][2] *= corr; acc[j][3] *= corr;
-        }
-      }
-      if (g < G) {
-        float* dst = sc + g * chunk_tok + (blk - blk0) * 16 + 2 * t;
-        *reinterpret_cast<float2*>(dst) = make_float2(sc4[0][0], sc4[0][1]);
-        *reinterpret_cast<float2*>(dst + 8) = make_float2(sc4[1][0], sc4[1][1]);
-      }
-      uint32_t pa[4];
-      {
-        __half hi[2][2], lo[2][2];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int j = 0; j < 2; ++j) split_hi_lo(p[nt][j], hi[nt][j], lo[nt][j]);
-        pa[0] = pack_h2(hi[0][0], hi[0][1]);
-        pa[1] = pack_h2(lo[0][0], lo[0][1]);
-        pa[2] = pack_h2(hi[1][0], hi[1][1]);
-        pa[3] = pack_h2(lo[1][0], lo[1][1]);
-      }
-#pragma unroll
-      for (int j = 0; j < D / 8; ++j) {
-        uint32_t b0, b1;
-        i8x4_to_h2x2(comp(vw[j >> 2], j & 3), b0, b1);
-        mma16816(acc[j], pa, b0, b1);
-      }
-    } else {
-      // ------------------------------------------------ FP16 ring block
-      constexpr int NC = D / 16;
-      const int rb = blk - nb8;
-      const uint4* kb = reinterpret_cast<const uint4*>(k16u + (size_t)rb * 32 * D);
-      const uint4* vb = reinterpret_cast<const uint4*>(v16u + (size_t)rb * 32 * D);
-      const int2 pv0 = *reinterpret_cast<const int2*>(posR + rb * 16 + 2 * t);
-      const int2 pv1 = *reinterpret_cast<const int2*>(posR + rb * 16 + 8 + 2 * t);
-      valid[0][0] = pv0.x >= 0; valid[0][1] = pv0.y >= 0;
-      valid[1][0] = pv1.x >= 0; valid[1][1] = pv1.y >= 0;
-      uint4 kw[NC];
-#pragma unroll
-      for (int r = 0; r < NC; ++r) kw[r] = __ldg(kb + r * 32 + lane);
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        float c[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint4& w4 = kw[nt * (D / 32) + (kk >> 1)];
-          mma16816(c, aq[kk], comp(w4, (kk & 1) * 2), comp(w4, (kk & 1) * 2 + 1));
-        }
-        sc4[nt][0] = (c[0] + c[2]) * kQPreInv;
-        sc4[nt][1] = (c[1] + c[3]) * kQPreInv;
-      }
-      float p[2][2];
-      {
-        float mloc = -INFINITY;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            if (!valid[nt][j] || g >= G) sc4[nt][j] = -INFINITY;
-            mloc = fmaxf(mloc, sc4[nt][j]);
-          }
-        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
-        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
-        const float m_new = fmaxf(m_run, mloc);
-        const float corr = (m_run == -INFINITY) ? 0.f : exp2f(m_run - m_new);
-        float ps = 0.f;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            p[nt][j] = (sc4[nt][j] == -INFINITY) ? 0.f : exp2f(sc4[nt][j] - m_new);
-            ps += p[nt][j];
-          }
-        l_run = l_run * corr + ps;
-        m_run = m_new;
-#pragma unroll
-        for (int j = 0; j < D / 8; ++j) {
-          acc[j][0] *= corr; acc[j][1] *= corr; acc[j][2] *= corr; acc[j][3] *= corr;
-        }
-      }
-      if (g < G) {
-        float* dst = sc + g * chunk_tok + (blk - blk0) * 16 + 2 * t;
-        *reinterpret_cast<float2*>(dst) = make_float2(sc4[0][0], sc4[0][1]);
-        *reinterpret_cast<float2*>(dst + 8) = make_float2(sc4[1][0], sc4[1][1]);
-      }
-      uint32_t pa[4];
-      {
-        __half hi[2][2], lo[2][2];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int j = 0; j < 2; ++j) split_hi_lo(p[nt][j], hi[nt][j], lo[nt][j]);
-        pa[0] = pack_h2(hi[0][0], hi[0][1]);
-        pa[1] = pack_h2(lo[0][0], lo[0][1]);
-        pa[2] = pack_h2(hi[1][0], hi[1][1]);
-        pa[3] = pack_h2(lo[1][0], lo[1][1]);
-      }
-      uint4 vw[NC];
-#pragma unroll
-      for (int r = 0; r < NC; ++r) vw[r] = __ldg(vb + r * 32 + lane);
-#pragma unroll
-      for (int j = 0; j < D / 8; ++j) {
-        const uint4& w4 = vw[j >> 1];
-        mma16816(acc[j], pa, comp(w4, (j & 1) * 2), comp(w4, (j & 1) * 2 + 1));
-      }
-    }
-  }
-  if (!in_ring) {
-#pragma unroll
-    for (int j = 0; j < D / 8; ++j) {
-      const float2 sv = *reinterpret_cast<const float2*>(sVu + j * 8 + 2 * t);
-      acc[j][0] *= sv.x; acc[j][1] *= sv.y; acc[j][2] *= sv.x; acc[j][3] *= sv.y;
-    }
-  }
-  // ---------------------------------------------------------------- warp -> CTA
-  l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
-  l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-  if (g < G) {
-    float* o = wo + (warp * G + g) * D;
-#pragma unroll
-    for (int j = 0; j < D / 8; ++j)
-      *reinterpret_cast<float2*>(o + j * 8 + 2 * t) =
-          make_float2(acc[j][0] + acc[j][2], acc[j][1] + acc[j][3]);
-    if (t == 0) {
-      wm[warp * G + g] = m_run;
-      wl[warp * G + g] = l_run;
-    }
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ------------------------------------------------ producer warp
+    if (lane == 0) {
+      int issued = 0;
+      for (int i = 0; i < sch.nst; ++i) {
+        const int slot = i % stages, use = i / stages;
+        if (use >= 1 && !mbar_wait(empty_bar(slot), (use - 1) & 1)) {
+          atomicOr(d.status, kStatusTimeout);
+          s_abort = 1;
+          break;
+        }
+        if (*(volatile int*)&s_abort) break;
+        bool ring;
+        int first, nb;
+        sch.first_last(i, ring, first, nb);
+        const uint32_t span = (uint32_t)(nb * 16 * D * (ring ? 2 : 1));
+        const char* ksrc = ring ? k16u + (size_t)first * 32 * D
+                                : reinterpret_cast<const char*>(k8u) + (size_t)first * 16 * D;
+        const char* vsrc = ring ? v16u + (size_t)first * 32 * D
+                                : reinterpret_cast<const char*>(v8u) + (size_t)first * 16 * D;
+        const uint32_t dst = smem_u32(sbuf + (size_t)slot * kStageBytes);
+        mbar_arrive_tx(full_bar(slot), 2 * span);
+        bulk_g2s(dst, ksrc, span, full_bar(slot));
+        bulk_g2s(dst + kHalf, vsrc, span, full_bar(slot));
+        issued = i + 1;
+      }
+      // drain: every issued copy must have landed before the CTA moves on
+      for (int i = max(0, issued - stages); i < issued; ++i) {
+        if (!mbar_wait(full_bar(i % stages), (i / stages) & 1)) atomicOr(d.status, kStatusTimeout);
+      }
+    }
+  } else {
+    // ------------------------------------------------ consumer warps
+    WarpState<D> ws;
+    const float qs = kQPre * 1.4426950408889634f * rsqrtf((float)D);
+    ws_begin<D>(ws, q, qoff, s.qbf16, sKu, qs, G, g, t);
+    for (int i = 0; i < sch.nst; ++i) {
+      const int slot = i % stages;
+      if (!mbar_wait(full_bar(slot), (i / stages) & 1)) {
+        if (lane == 0) atomicOr(d.status, kStatusTimeout);
+        s_abort = 1;
+        break;
+      }
+      if (*(volatile int*)&s_abort) break;
+      bool ring;
+      int first, nb;
+      sch.first_last(i, ring, first, nb);
+      const uint32_t stage = smem_u32(sbuf + (size_t)slot * kStageBytes);
+      if (!ring) {
+        if (warp < nb) {
+          const int blk = first + warp;
+          int8_block<D>(ws, stage + warp * 16 * D, stage + kHalf + warp * 16 * D, blk, n8, G, g, t,
+                        lane, sc + g * chunk_tok + (blk - blk0) * 16 + 2 * t);
+        }
+      } else {
+        const int jb = warp - 2 * ((i - sch.n8st) & 1);
+        if (jb >= 0 && jb < nb) {
+          if (!ws.in_ring) ws_to_ring<D>(ws, q, qoff, s.qbf16, qs, sVu, G, g, t);
+          const int rb = first + jb;
+          ring_block<D>(ws, stage + jb * 32 * D, stage + kHalf + jb * 32 * D, posR + rb * 16, G, g,
+                        t, lane, sc + g * chunk_tok + (nb8 + rb - blk0) * 16 + 2 * t);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar(slot));
+    }
+    ws_store<D>(ws, sVu, G, g, t, wm + warp * G, wl + warp * G, wo + warp * G * D);
+  }
+  __syncthreads();
+  const bool aborted = s_abort != 0;
   for (int i = threadIdx.x; i < G * D; i += kAttnThreads) {
     const int gg = i / D, c = i % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kAttnWarps; ++w) M = fmaxf(M, wm[w * G + gg]);
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, wm[w * G + gg]);
     float o = 0.f, L = 0.f;
 #pragma unroll
-    for (int w = 0; w < kAttnWarps; ++w) {
+    for (int w = 0; w < kConsumerWarps; ++w) {
       const float mw = wm[w * G + gg];
-      const float f = (mw == -INFINITY) ? 0.f : exp2f(mw - M);
+      const float f = (mw == -INFINITY) ? 0.f : ex2(mw - M);
       o += wo[(w * G + gg) * D + c] * f;
       L += wl[w * G + gg] * f;
     }
@@ -388,66 +580,522 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(Shape s, Dev d,
     float L = 0.f;
     for (int r = 0; r < splits; ++r) {
       const float mr = cluster.map_shared_rank(cm, r)[gg];
-      if (mr != -INFINITY) L += cluster.map_shared_rank(cl, r)[gg] * exp2f(mr - M);
+      if (mr != -INFINITY) L += cluster.map_shared_rank(cl, r)[gg] * ex2(mr - M);
     }
     gM[gg] = M;
     gL[gg] = L;
   }
   __syncthreads();
-  // attention mass of this CTA's tokens, summed over its G query heads
-  float* mass_u = d.mass + (size_t)u * s.S;
-  const int ntok = (blk1 - blk0) * 16;
-  for (int i = threadIdx.x; i < ntok; i += kAttnThreads) {
-    const float s0 = sc[i];
-    if (s0 == -INFINITY) continue;   // empty ring slot or tail past n8
-    float m = 0.f;
-    for (int gg = 0; gg < G; ++gg) m += exp2f(sc[gg * chunk_tok + i] - gM[gg]) / gL[gg];
-    const int blk = blk0 + (i >> 4);
-    const int slot = blk < nb8 ? blk * 16 + (i & 15) : s.cap + (blk - nb8) * 16 + (i & 15);
-    mass_u[slot] = m;
-  }
-  if (rank == 0) {
-    float* o = out + qoff;
-    for (int i = threadIdx.x; i < G * D; i += kAttnThreads) {
-      const int gg = i / D;
-      float acc_o = 0.f;
-      for (int r = 0; r < splits; ++r) {
-        const float mr = cluster.map_shared_rank(cm, r)[gg];
-        if (mr != -INFINITY) acc_o += cluster.map_shared_rank(co, r)[i] * exp2f(mr - gM[gg]);
+  if (!aborted) {
+    // attention mass of this CTA's tokens, summed over its G query heads
+    float* mass_u = d.mass + (size_t)u * s.S;
+    const int ntok = (blk1 - blk0) * 16;
+    for (int i = threadIdx.x; i < ntok; i += kAttnThreads) {
+      const float s0 = sc[i];
+      if (s0 == -INFINITY) continue;   // empty ring slot or tail past n8
+      float m = 0.f;
+      for (int gg = 0; gg < G; ++gg) m += ex2(sc[gg * chunk_tok + i] - gM[gg]) / gL[gg];
+      const int blk = blk0 + (i >> 4);
+      const int slot = blk < nb8 ? blk * 16 + (i & 15) : s.cap + (blk - nb8) * 16 + (i & 15);
+      mass_u[slot] = m;
+    }
+    if (rank == 0) {
+      float* o = out + qoff;
+      for (int i = threadIdx.x; i < G * D; i += kAttnThreads) {
+        const int gg = i / D;
+        float acc_o = 0.f;
+        for (int r = 0; r < splits; ++r) {
+          const float mr = cluster.map_shared_rank(cm, r)[gg];
+          if (mr != -INFINITY) acc_o += cluster.map_shared_rank(co, r)[i] * ex2(mr - gM[gg]);
+        }
+        o[i] = acc_o / gL[gg];
       }
-      o[i] = acc_o / gL[gg];
     }
   }
   cluster.sync();   // peers keep their shared memory alive until rank 0 has read it
 }
 
-int attention_smem_bytes(const Shape& s, int splits, int max_tokens) {
-  const int nbT = (max_tokens + 15) / 16;
-  const int chunk = (nbT + splits - 1) / splits;
-  const int G = s.G, D = s.D;
-  size_t f = (size_t)G * chunk * 16 + 2 * kAttnWarps * G + (size_t)kAttnWarps * G * D + 2 * kMaxG +
-             (size_t)G * D + 2 * kMaxG;
-  return (int)(f * sizeof(float));
+// ===========================================================================
+// Persistent kernel: two CTAs per SM walk the units u = blockIdx.x,
+// blockIdx.x + gridDim.x, ...  Each CTA has three roles:
+//   producer warp   streams, unit after unit without stopping, a small unit
+//                   header (query rows, K and V scales, ring positions) and
+//                   the unit's K/V blocks into shared memory (1-D TMA bulk
+//                   copies completing on mbarriers; K/V with an evict-first
+//                   L2 hint);
+//   4 consumer warps take one block of every stage and keep the online
+//                   softmax state; the raw scores go to this CTA's slot of a
+//                   global scratch buffer (evict-last: it is rewritten every
+//                   unit and stays in L2);
+//   epilogue warp   merges the consumers' partial results of unit u, writes
+//                   the output and the per-token attention mass, while the
+//                   consumers already work on unit u + 1.
+// The per-unit buffers handed to the epilogue (partials, score slot) and the
+// unit header are double-buffered.  Every mbarrier wait is bounded.
+// ===========================================================================
+constexpr int kPConsumers = 4;
+constexpr int kPThreads = (kPConsumers + 2) * 32;
+constexpr int kPMaxStages = 12;
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;\n" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;\n" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;\n" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+      : "memory");
 }
 
-int attention_max_smem() { return 200 * 1024; }
+// Shared-memory header of one unit (byte offsets).
+struct HeaderLayout {
+  int q, sk, sv, pos, bytes;
+  __host__ __device__ HeaderLayout(int G, int D, int WR) {
+    q = 0;
+    sk = (G * D * 2 + 15) / 16 * 16;
+    sv = sk + D * 4;
+    pos = sv + D * 4;
+    bytes = (pos + WR * 4 + 127) / 128 * 128;
+  }
+};
+
+// Query A fragments built from the header copy of q (2-byte elements) and,
+// for INT8 blocks, the K scales.  Same layout as make_q_frag.
+template <int D>
+__device__ __forceinline__ float make_q_frag_s(uint32_t (&aq)[D / 16][4], const unsigned char* qh,
+                                               int bf16, const float* ksc, float qs, int G, int g,
+                                               int t) {
+  float sum = 0.f;
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    float x[4] = {0.f, 0.f, 0.f, 0.f};
+    if (g < G) {
+      const int c0 = kk * 16 + 2 * t;
+      const int cs[4] = {c0, c0 + 1, c0 + 8, c0 + 9};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float sc = ksc ? ksc[cs[e]] : 1.0f;
+        const unsigned short raw = reinterpret_cast<const unsigned short*>(qh)[g * D + cs[e]];
+        const float qv = bf16 ? __uint_as_float((uint32_t)raw << 16)
+                              : __half2float(__ushort_as_half(raw));
+        x[e] = qv * sc * qs;
+      }
+    }
+    __half h[4], lo[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      split_hi_lo(x[e], h[e], lo[e]);
+      sum += __half2float(h[e]) + __half2float(lo[e]);
+    }
+    aq[kk][0] = pack_h2(h[0], h[1]);
+    aq[kk][1] = pack_h2(lo[0], lo[1]);
+    aq[kk][2] = pack_h2(h[2], h[3]);
+    aq[kk][3] = pack_h2(lo[2], lo[3]);
+  }
+  sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+  sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+  return 1152.0f * sum;
+}
+
+// Ring of `n` slots with a phase bit that flips on every wrap.
+struct RingPos {
+  int slot = 0;
+  uint32_t phase = 0;
+  __device__ void next(int n) {
+    if (++slot == n) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
+    Shape s, Dev d, const void* __restrict__ q, float* __restrict__ out, int stages) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  constexpr int kStageBytes = 128 * D;
+  constexpr int kHalf = kStageBytes / 2;
+  const int G = s.G;
+  const HeaderLayout hl(G, D, s.WR);
+  unsigned char* sbuf = smem_raw;                                          // [stages][kStageBytes]
+  unsigned char* hbuf = smem_raw + (size_t)stages * kStageBytes;           // [2][hl.bytes]
+  float* wpart = reinterpret_cast<float*>(hbuf + 2 * hl.bytes);            // [2][4][G][D + 2]
+  const int part_floats = kPConsumers * G * (D + 2);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(wpart + 2 * part_floats);
+  int& s_abort = *reinterpret_cast<int*>(bars + 2 * kPMaxStages + 8);
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
+  auto empty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(kPMaxStages + i); };
+  auto hfull_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * kPMaxStages + i); };
+  auto hempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * kPMaxStages + 2 + i); };
+  auto done_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * kPMaxStages + 4 + i); };
+  auto efree_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * kPMaxStages + 6 + i); };
+  // this CTA's two score slots: [2][G][S] (token index = slot index in the unit)
+  float* scg_base = d.scores + (size_t)blockIdx.x * 2 * G * s.S;
+
+  const int units = s.L * s.B * s.Hkv;
+  const int nbR = s.WR >> 4;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int i = 0; i < stages; ++i) {
+      mbar_init(full_bar(i), 1);
+      mbar_init(empty_bar(i), kPConsumers);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(hfull_bar(i), 1);
+      mbar_init(hempty_bar(i), kPConsumers);
+      mbar_init(done_bar(i), kPConsumers);
+      mbar_init(efree_bar(i), 1);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+
+  auto fail = [&](void) {
+    atomicOr(d.status, kStatusTimeout);
+    s_abort = 1;
+  };
+  auto aborted = [&](void) { return *(volatile int*)&s_abort != 0; };
+
+  if (warp == kPConsumers) {
+    // ------------------------------------------------ producer warp
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      RingPos st;
+      long long issued = 0;
+      int k = 0;
+      for (int u = blockIdx.x; u < units && !aborted(); u += gridDim.x, ++k) {
+        const int h = u % s.Hkv, b = (u / s.Hkv) % s.B, l = u / (s.Hkv * s.B);
+        const size_t lb = lb_index(s, l, b);
+        const int nb8 = (d.n8[lb] + 15) >> 4;
+        // unit header
+        const int hs = k & 1;
+        if (k >= 2 && !mbar_wait(hempty_bar(hs), (uint32_t)(((k >> 1) - 1) & 1))) { fail(); break; }
+        const uint32_t hdst = smem_u32(hbuf + (size_t)hs * hl.bytes);
+        const uint32_t qbytes = (uint32_t)(G * D * 2);
+        mbar_arrive_tx(hfull_bar(hs), qbytes + 2u * D * 4 + (uint32_t)s.WR * 4);
+        bulk_g2s(hdst + hl.q, reinterpret_cast<const char*>(q) + (lb * s.Hq + (size_t)h * G) * D * 2,
+                 qbytes, hfull_bar(hs));
+        bulk_g2s(hdst + hl.sk, d.sK + (size_t)u * D, D * 4, hfull_bar(hs));
+        bulk_g2s(hdst + hl.sv, d.sV + (size_t)u * D, D * 4, hfull_bar(hs));
+        bulk_g2s(hdst + hl.pos, d.pos + lb * s.S + s.cap, (uint32_t)s.WR * 4, hfull_bar(hs));
+        // K/V stages
+        Sched sch;
+        sch.init(0, nb8 + nbR, nb8);
+        const char* k8u = reinterpret_cast<const char*>(d.k8) + (size_t)u * s.cap * D;
+        const char* v8u = reinterpret_cast<const char*>(d.v8) + (size_t)u * s.cap * D;
+        const char* k16u = reinterpret_cast<const char*>(d.k16) + (size_t)u * s.WR * D * 2;
+        const char* v16u = reinterpret_cast<const char*>(d.v16) + (size_t)u * s.WR * D * 2;
+        bool ok = true;
+        for (int i = 0; i < sch.nst; ++i) {
+          if (issued >= stages && !mbar_wait(empty_bar(st.slot), st.phase ^ 1u)) { ok = false; break; }
+          bool ring;
+          int first, nb;
+          sch.first_last(i, ring, first, nb);
+          const uint32_t span = (uint32_t)(nb * 16 * D * (ring ? 2 : 1));
+          const char* ksrc = ring ? k16u + (size_t)first * 32 * D : k8u + (size_t)first * 16 * D;
+          const char* vsrc = ring ? v16u + (size_t)first * 32 * D : v8u + (size_t)first * 16 * D;
+          const uint32_t dst = smem_u32(sbuf + (size_t)st.slot * kStageBytes);
+          mbar_arrive_tx(full_bar(st.slot), 2 * span);
+          bulk_g2s_hint(dst, ksrc, span, full_bar(st.slot), pol);
+          bulk_g2s_hint(dst + kHalf, vsrc, span, full_bar(st.slot), pol);
+          st.next(stages);
+          ++issued;
+        }
+        if (!ok) { fail(); break; }
+      }
+      // wait (bounded) for the last copy of every stage slot: nothing may be
+      // in flight into shared memory when the CTA's threads have all exited
+      RingPos dr = st;
+      for (int i = 0; i < stages && i < issued; ++i) {
+        dr.slot = dr.slot == 0 ? stages - 1 : dr.slot - 1;
+        if (dr.slot == stages - 1) dr.phase ^= 1u;
+        if (!mbar_wait(full_bar(dr.slot), dr.phase)) atomicOr(d.status, kStatusTimeout);
+      }
+    }
+    return;
+  }
+
+  if (warp == kPConsumers + 1) {
+    // ------------------------------------------------ epilogue warp
+    int k = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x, ++k) {
+      const int ps = k & 1;
+      if (aborted() || !mbar_wait(done_bar(ps), (uint32_t)((k >> 1) & 1))) {
+        if (!aborted()) fail();
+        break;
+      }
+      const int h = u % s.Hkv, b = (u / s.Hkv) % s.B, l = u / (s.Hkv * s.B);
+      const size_t lb = lb_index(s, l, b);
+      const int nb8 = (d.n8[lb] + 15) >> 4;
+      const float* part = wpart + (size_t)ps * part_floats;   // [4][G][D + 2]: o..., m, l
+      float Mg[kMaxG], Lg[kMaxG], fw[kPConsumers][kMaxG];
+#pragma unroll
+      for (int gg = 0; gg < kMaxG; ++gg) {
+        Mg[gg] = -INFINITY;
+        Lg[gg] = 0.f;
+        if (gg < G) {
+#pragma unroll
+          for (int w = 0; w < kPConsumers; ++w) Mg[gg] = fmaxf(Mg[gg], part[(w * G + gg) * (D + 2) + D]);
+#pragma unroll
+          for (int w = 0; w < kPConsumers; ++w) {
+            const float mw = part[(w * G + gg) * (D + 2) + D];
+            fw[w][gg] = (mw == -INFINITY) ? 0.f : ex2(mw - Mg[gg]);
+            Lg[gg] += part[(w * G + gg) * (D + 2) + D + 1] * fw[w][gg];
+          }
+        }
+      }
+      // output
+      float* o = out + (lb * s.Hq + (size_t)h * G) * D;
+#pragma unroll
+      for (int gg = 0; gg < kMaxG; ++gg) {
+        if (gg < G) {
+          const float inv = 1.0f / Lg[gg];
+          for (int c = lane; c < D; c += 32) {
+            float acc = 0.f;
+#pragma unroll
+            for (int w = 0; w < kPConsumers; ++w) acc += part[(w * G + gg) * (D + 2) + c] * fw[w][gg];
+            o[gg * D + c] = acc * inv;
+          }
+        }
+      }
+      // attention mass, 4 consecutive slots per lane (slot groups never
+      // straddle the INT8 / ring boundary); empty slots get 0 (never read)
+      const float* scg = scg_base + (size_t)ps * G * s.S;
+      float* mass_u = d.mass + (size_t)u * s.S;
+      const int nq = (nb8 * 16 + s.WR) / 4;
+      float invL[kMaxG];
+#pragma unroll
+      for (int gg = 0; gg < kMaxG; ++gg) invL[gg] = gg < G ? 1.0f / Lg[gg] : 0.f;
+      for (int i = lane; i < nq; i += 32) {
+        const int v = 4 * i;
+        const int slot = v < nb8 * 16 ? v : s.cap + (v - nb8 * 16);
+        float4 sv[kMaxG];
+#pragma unroll
+        for (int gg = 0; gg < kMaxG; ++gg)
+          if (gg < G) sv[gg] = *reinterpret_cast<const float4*>(scg + (size_t)gg * s.S + slot);
+        float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int gg = 0; gg < kMaxG; ++gg) {
+          if (gg < G) {
+            m.x += ex2(sv[gg].x - Mg[gg]) * invL[gg];
+            m.y += ex2(sv[gg].y - Mg[gg]) * invL[gg];
+            m.z += ex2(sv[gg].z - Mg[gg]) * invL[gg];
+            m.w += ex2(sv[gg].w - Mg[gg]) * invL[gg];
+          }
+        }
+        *reinterpret_cast<float4*>(mass_u + slot) = m;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(efree_bar(ps));
+    }
+    return;
+  }
+
+  // -------------------------------------------------- consumer warps
+  const float qs = kQPre * 1.4426950408889634f * rsqrtf((float)D);
+  const uint64_t keep = policy_evict_last();
+  RingPos st;
+  int k = 0;
+  for (int u = blockIdx.x; u < units; u += gridDim.x, ++k) {
+    const int hs = k & 1;
+    if (aborted() || !mbar_wait(hfull_bar(hs), (uint32_t)((k >> 1) & 1))) {
+      if (!aborted()) fail();
+      break;
+    }
+    if (k >= 2 && !mbar_wait(efree_bar(hs), (uint32_t)(((k >> 1) - 1) & 1))) {
+      fail();
+      break;
+    }
+    const int b = (u / s.Hkv) % s.B, l = u / (s.Hkv * s.B);
+    const size_t lb = lb_index(s, l, b);
+    const int n8 = d.n8[lb];
+    const int nb8 = (n8 + 15) >> 4;
+    const unsigned char* hdr = hbuf + (size_t)hs * hl.bytes;
+    const float* sKh = reinterpret_cast<const float*>(hdr + hl.sk);
+    const float* sVh = reinterpret_cast<const float*>(hdr + hl.sv);
+    const int32_t* posh = reinterpret_cast<const int32_t*>(hdr + hl.pos);
+    float* scg = scg_base + (size_t)hs * G * s.S;
+    Sched sch;
+    sch.init(0, nb8 + nbR, nb8);
+    WarpState<D> ws;
+    ws.qoffset = make_q_frag_s<D>(ws.aq, hdr + hl.q, s.qbf16, sKh, qs, G, g, t);
+#pragma unroll
+    for (int j = 0; j < D / 8; ++j) ws.acc[j][0] = ws.acc[j][1] = ws.acc[j][2] = ws.acc[j][3] = 0.f;
+    ws.m_run = -INFINITY;
+    ws.l_run = 0.f;
+    ws.in_ring = false;
+    float sc4buf[4];
+    bool ok = true;
+    for (int i = 0; i < sch.nst; ++i) {
+      if (!mbar_wait(full_bar(st.slot), st.phase)) { ok = false; break; }
+      bool ring;
+      int first, nb;
+      sch.first_last(i, ring, first, nb);
+      const uint32_t stage = smem_u32(sbuf + (size_t)st.slot * kStageBytes);
+      int tok0 = -1;
+      if (!ring) {
+        if (warp < nb) {
+          const int blk = first + warp;
+          tok0 = blk * 16;
+          int8_block<D>(ws, stage + warp * 16 * D, stage + kHalf + warp * 16 * D, blk, n8, G, g, t,
+                        lane, nullptr, sc4buf);
+        }
+      } else if (warp < nb) {
+        if (!ws.in_ring) {
+          make_q_frag_s<D>(ws.aq, hdr + hl.q, s.qbf16, nullptr, qs, G, g, t);
+          ws.qoffset = 0.f;
+          ws_scale_v<D>(ws, sVh, t);
+          ws.in_ring = true;
+        }
+        const int rb = first + warp;
+        tok0 = s.cap + rb * 16;
+        ring_block<D>(ws, stage + warp * 32 * D, stage + kHalf + warp * 32 * D, posh + rb * 16, G, g, t,
+                      lane, nullptr, sc4buf);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar(st.slot));
+      st.next(stages);
+      if (tok0 >= 0 && g < G) {
+        // raw scores of tokens tok0 + {2t, 2t+1, 8+2t, 9+2t} of head g
+        float* dst = scg + (size_t)g * s.S + tok0 + 2 * t;
+        asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;\n" ::"l"(dst),
+                     "f"(sc4buf[0]), "f"(sc4buf[1]), "l"(keep) : "memory");
+        asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;\n" ::"l"(dst + 8),
+                     "f"(sc4buf[2]), "f"(sc4buf[3]), "l"(keep) : "memory");
+      }
+    }
+    if (!ok) {
+      fail();
+      break;
+    }
+    // partials of this warp -> the epilogue warp: [4][G][D + 2] = o..., m, l
+    if (!ws.in_ring) ws_scale_v<D>(ws, sVh, t);
+    float lsum = ws.l_run;
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+    if (g < G) {
+      float* pw = wpart + (size_t)hs * part_floats + (size_t)(warp * G + g) * (D + 2);
+#pragma unroll
+      for (int j = 0; j < D / 8; ++j) {
+        pw[j * 8 + 2 * t] = ws.acc[j][0] + ws.acc[j][2];
+        pw[j * 8 + 2 * t + 1] = ws.acc[j][1] + ws.acc[j][3];
+      }
+      if (t == 0) {
+        pw[D] = ws.m_run;
+        pw[D + 1] = lsum;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(done_bar(hs));
+      mbar_arrive(hempty_bar(hs));
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Launch shapes
+// ---------------------------------------------------------------------------
+static int stage_bytes(int D) { return 128 * D; }
+
+static int chunk_of(int splits, int max_tokens) {
+  const int nbT = (max_tokens + 15) / 16;
+  return (nbT + splits - 1) / splits;
+}
+
+static int fixed_bytes_split(const Shape& s, int splits, int max_tokens) {
+  const int chunk = chunk_of(splits, max_tokens);
+  const int G = s.G, D = s.D;
+  size_t f = (size_t)G * chunk * 16 + 2 * kConsumerWarps * G + (size_t)kConsumerWarps * G * D +
+             2 * kMaxG + (size_t)G * D + 2 * kMaxG + 4;
+  return (int)(f * sizeof(float)) + 2 * kMaxStages * 8;
+}
+
+static int fixed_bytes_persistent(const Shape& s) {
+  const HeaderLayout hl(s.G, s.D, s.WR);
+  const int part = kPConsumers * s.G * (s.D + 2) * 4;
+  return 2 * hl.bytes + 2 * part + (2 * kPMaxStages + 8) * 8 + 16;
+}
+
+int attention_max_smem() { return 225 * 1024; }
+
+// Split kernel: as many stages as fit while two CTAs share an SM.
+static int stages_split(const Shape& s, int splits, int max_tokens) {
+  int st = (113 * 1024 - fixed_bytes_split(s, splits, max_tokens)) / stage_bytes(s.D);
+  return st > kMaxStages ? kMaxStages : (st < 2 ? 2 : st);
+}
+
+// Persistent kernel: as many stages as fit while two CTAs share an SM.
+static int stages_persistent(const Shape& s) {
+  int st = (113 * 1024 - fixed_bytes_persistent(s)) / stage_bytes(s.D);
+  return st > kPMaxStages ? kPMaxStages : (st < 2 ? 2 : st);
+}
+
+int attention_smem_bytes(const Shape& s, int splits, int max_tokens) {
+  if (splits == 1) return stages_persistent(s) * stage_bytes(s.D) + fixed_bytes_persistent(s);
+  return stages_split(s, splits, max_tokens) * stage_bytes(s.D) +
+         fixed_bytes_split(s, splits, max_tokens);
+}
+
+int attention_persistent_ctas();
+
+static int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 152;
+  }
+  return n;
+}
+
+int attention_persistent_ctas() { return 2 * num_sms(); }
 
 template <int D>
 static int launch_d(const Shape& s, const Dev& d, const void* q, float* out, int splits,
                     int max_tokens, cudaStream_t stream) {
-  const int nbT = (max_tokens + 15) / 16;
-  const int chunk = (nbT + splits - 1) / splits;
+  const int chunk = chunk_of(splits, max_tokens);
   const int smem = attention_smem_bytes(s, splits, max_tokens);
-  static int configured = 0;
-  if (smem > configured) {
+  if (smem > attention_max_smem()) return -1;
+  const int units = s.L * s.B * s.Hkv;
+  if (splits == 1) {
+    static bool configured = false;
+    if (!configured) {
+      if (cudaFuncSetAttribute(attention_persistent_kernel<D>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               attention_max_smem()) != cudaSuccess)
+        return -1;
+      configured = true;
+    }
+    int grid = units < 2 * num_sms() ? units : 2 * num_sms();
+    if (grid > d.score_ctas) grid = d.score_ctas;
+    attention_persistent_kernel<D><<<grid, kPThreads, smem, stream>>>(
+        s, d, q, out, stages_persistent(s));
+    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+  }
+  static bool configured_split = false;
+  if (!configured_split) {
     if (cudaFuncSetAttribute(attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              attention_max_smem()) != cudaSuccess)
       return -1;
-    configured = attention_max_smem();
+    configured_split = true;
   }
-  const unsigned units = (unsigned)(s.L * s.B * s.Hkv);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(units * splits);
+  cfg.gridDim = dim3((unsigned)units * splits);
   cfg.blockDim = dim3(kAttnThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
@@ -458,7 +1106,8 @@ static int launch_d(const Shape& s, const Dev& d, const void* q, float* out, int
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, attention_kernel<D>, s, d, q, out, splits, chunk);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attention_kernel<D>, s, d, q, out, splits, chunk,
+                                     stages_split(s, splits, max_tokens));
   return e == cudaSuccess ? 0 : -1;
 }
 

@@ -11,7 +11,8 @@
 //   Attention-mass partials [l][b][kvh][S] (fp32, one per KV head).
 //
 //   K/V payload per unit u = (l, b, kvh), in 16-token blocks:
-//     INT8:  k8, v8  [u][cap/16][16*D bytes]
+//     INT8:  k8, v8  [u][cap/16][16*D bytes], each byte the code + 128
+//                    (code in [-127, 127], stored biased as uint8)
 //     FP16:  k16,v16 [u][WR/16][16*D halves]
 //   Inside a block the bytes are interleaved so that lane `lane` of a warp
 //   reading 16 contiguous bytes at  r*512 + lane*16  receives exactly its
@@ -26,6 +27,7 @@ namespace confkv {
 constexpr int kRingExtra = 16;      // WR = W + kRingExtra
 constexpr int kMaxG = 8;            // query heads per KV head supported
 constexpr int kMaxSV = 1024;        // confidence partial blocks per sequence
+constexpr int kCodeBias = 128;      // stored INT8 byte = code + 128
 
 // ---------------------------------------------------------------------------
 // Block interleave (host and device).  tau in [0,16) is the token within the
@@ -105,7 +107,7 @@ struct Shape {
 };
 
 struct Dev {
-  int8_t* k8;  int8_t* v8;
+  uint8_t* k8; uint8_t* v8;        // biased INT8 codes (code + 128)
   __half* k16; __half* v16;
   float* sK;   float* sV;          // [l][b][kvh][D]
   int32_t* pos; float* ema;        // [l][b][S]
@@ -118,6 +120,8 @@ struct Dev {
   DevStats* stats;
   int32_t* status;                 // device status word (0 = ok)
   uint32_t* absmax;                // [2][l][b][kvh][D] prefill scratch
+  float* scores;                   // [persistent CTAs][2][G][S] attention score scratch
+  int score_ctas;                  // persistent attention CTAs the score scratch holds
 };
 
 // Status bits written by kernels (never trap; the host reads them lazily).
@@ -126,6 +130,7 @@ enum : int32_t {
   kStatusCapacity = 1,     // an INT8 region would overflow
   kStatusEvictBound = 2,   // more evictions than the evicted_pos rows hold
   kStatusBadCount = 4,     // inconsistent eviction count (selection failed)
+  kStatusTimeout = 8,      // a bounded mbarrier wait gave up
 };
 
 __host__ __device__ inline size_t unit_index(const Shape& s, int l, int b, int h) {
@@ -148,5 +153,6 @@ int launch_select(const Shape& s, const Dev& d, long long step, int32_t* budget,
                   int32_t* evicted_pos, int32_t* n_evicted, int k_bound, cudaStream_t stream);
 int attention_smem_bytes(const Shape& s, int splits, int max_tokens);
 int attention_max_smem();
+int attention_persistent_ctas();   // persistent CTAs per launch (2 per SM)
 
 }  // namespace confkv

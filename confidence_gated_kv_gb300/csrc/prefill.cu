@@ -17,10 +17,11 @@ __device__ __forceinline__ float scale_from_absmax(uint32_t bits) {
   return a > 0.f ? __fdiv_rn(a, 127.0f) : 1.0f;
 }
 
-__device__ __forceinline__ int8_t quant_code(float x, float s) {
+// Stored byte of code = clamp(rint(x / s), -127, 127): the code + 128.
+__device__ __forceinline__ uint8_t quant_code(float x, float s) {
   float r = rintf(__fdiv_rn(x, s));
   r = fminf(fmaxf(r, -127.f), 127.f);
-  return (int8_t)(int)r;
+  return (uint8_t)((int)r + kCodeBias);
 }
 
 // grid: (units, token splits); block: D threads (one channel each).
@@ -109,8 +110,8 @@ int launch_prefill(const Shape& s, const Dev& d, const void* k, const void* v, l
   cudaMemsetAsync(d.ema, 0, (size_t)s.L * s.B * s.S * sizeof(float), stream);
   cudaMemsetAsync(d.k16, 0, units * s.WR * s.D * sizeof(__half), stream);
   cudaMemsetAsync(d.v16, 0, units * s.WR * s.D * sizeof(__half), stream);
-  cudaMemsetAsync(d.k8, 0, units * (size_t)s.cap * s.D, stream);
-  cudaMemsetAsync(d.v8, 0, units * (size_t)s.cap * s.D, stream);
+  cudaMemsetAsync(d.k8, kCodeBias, units * (size_t)s.cap * s.D, stream);
+  cudaMemsetAsync(d.v8, kCodeBias, units * (size_t)s.cap * s.D, stream);
   // Sequences with T0 = 0 still need their scales (1.0) and n8 = 0.
   int tsplit = tmax0 > 0 ? (tmax0 + 1023) / 1024 : 1;
   if (tsplit > 64) tsplit = 64;

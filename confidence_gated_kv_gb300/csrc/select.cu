@@ -30,10 +30,11 @@ namespace confkv {
 constexpr int kSelThreads = 512;
 constexpr int kSelWarps = kSelThreads / 32;
 
-__device__ __forceinline__ int8_t quant_code_sel(float x, float s) {
+// Stored byte of code = clamp(rint(x / s), -127, 127): the code + 128.
+__device__ __forceinline__ uint8_t quant_code_sel(float x, float s) {
   float r = rintf(__fdiv_rn(x, s));
   r = fminf(fmaxf(r, -127.f), 127.f);
-  return (int8_t)(int)r;
+  return (uint8_t)((int)r + kCodeBias);
 }
 
 template <typename T, typename Op>
@@ -358,8 +359,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(Shape s, Dev d, lon
       const int h = rest / per_tok, e = rest % per_tok;
       const int src = (int)mover[r], dst = (int)hole[r];
       const size_t u = unit_index(s, l, b, h);
-      int8_t* k8u = d.k8 + u * (size_t)s.cap * D;
-      int8_t* v8u = d.v8 + u * (size_t)s.cap * D;
+      uint8_t* k8u = d.k8 + u * (size_t)s.cap * D;
+      uint8_t* v8u = d.v8 + u * (size_t)s.cap * D;
       if (e < D / 4) {
         // one 32-bit word = channels {16kk+2t, +1, +8, +9} of the token
         const int kk = e / 4, tq = e % 4;

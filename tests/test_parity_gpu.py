@@ -143,7 +143,9 @@ def test_capacity_is_checked_before_launch():
     k, v = prefill_batch(w, 18, "cpu")
     c = ck.Cache(ck.config_from_workload(w))
     c.prefill(k.cuda(), v.cuda(), [40])
-    for s in range(16):
+    # 32 INT8 entries after prefill, one more per step: the 17th step would
+    # need slot 48 of a 48-slot region
+    for s in range(40):
         try:
             c.step(*(t.cuda() for t in step_inputs(w, 18, s)))
         except ck.ConfkvError as e:

@@ -88,6 +88,8 @@ def lib() -> ctypes.CDLL:
                                     [ctypes.POINTER(i32)]),
             "confkv_attention_plan": (ctypes.c_int, [vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]),
             "confkv_block_offset": (i32, [i32, i32, i32, i32]),
+            "confkv_confidence_noalloc": (ctypes.c_int, [vp, i32, i32, ctypes.c_double, ctypes.c_double,
+                                                         ctypes.c_double, vp, vp]),
             "confkv_status_string": (ctypes.c_char_p, [ctypes.c_int]),
             "confkv_version": (i32, []),
         }
@@ -105,6 +107,17 @@ def status_string(status: int) -> str:
 
 def block_offset(kind: int, d: int, tau: int, c: int) -> int:
     return int(lib().confkv_block_offset(kind, d, tau, c))
+
+
+def confidence_noalloc(logits, out, w_H: float = 0.4, w_m: float = 0.3, w_p: float = 0.3,
+                       stream=None):
+    """Confidence of each row of `logits` (device fp32 [B][V]) into `out`
+    (device fp32 [B]) through confkv_confidence_noalloc, which allocates no
+    device memory (see include/confkv.h)."""
+    B, V = int(logits.shape[0]), int(logits.shape[1])
+    _check(lib().confkv_confidence_noalloc(_ptr(logits), B, V, w_H, w_m, w_p, _ptr(out),
+                                           _stream(stream)), "confkv_confidence_noalloc")
+    return out
 
 
 def _check(status: int, what: str):

@@ -220,6 +220,38 @@ int confkv_attention_plan(confkv_ctx* ctx, int32_t* splits, int32_t* smem_bytes)
  * Host-only helper for tests of the interleave; -1 for bad arguments. */
 int32_t confkv_block_offset(int32_t kind, int32_t d, int32_t tau, int32_t c);
 
+/* Largest number of per-chunk partial results confkv_confidence_noalloc can
+ * hold: B * ceil(V / 4096) must not exceed it.  The library reserves this
+ * scratch (32 bytes per partial, 128 KiB) on every GPU that loads it, for as
+ * long as the process runs. */
+#define CONFKV_NOALLOC_MAX_PARTIALS 4096
+
+/*
+ * Confidence c of B next-token distributions, computed without allocating
+ * any device memory.  The paper has no counterpart of this call: it exists
+ * for callers that cannot allocate where they need the score -- a plug-in
+ * whose host process owns every device buffer through its own pool, a
+ * real-time loop that forbids allocation after start-up, or code that must
+ * not risk the implicit synchronisation an allocation can cause.  The caller
+ * passes only its input and output:
+ *   logits      device fp32 [B][V] (temperature 1)
+ *   confidence  device fp32 [B], written: the same c as the `confidence`
+ *               output of confkv_step, c = w_H (1 - H / log V) +
+ *               w_m sigmoid(log p1 - log p2) + w_p p1
+ * The partial results of the vocabulary reduction go to one fixed scratch
+ * array owned by the library (CONFKV_NOALLOC_MAX_PARTIALS entries per GPU).
+ * Every call uses that same array and leaves its last contents there, so
+ * calls whose kernels overlap on the GPU (streams without ordering between
+ * them) race and give wrong results; order them on one stream.  The first
+ * call on a device looks up the array's device address (once per device,
+ * with that device current); make that first call before any stream capture.
+ * Returns CONFKV_ECAPACITY, without launching anything, if
+ * B * ceil(V / 4096) > CONFKV_NOALLOC_MAX_PARTIALS; CONFKV_EINVAL for null
+ * pointers, B < 1, V < 2 or non-finite weights.  Asynchronous on `stream`.
+ */
+int confkv_confidence_noalloc(const float* logits, int32_t B, int32_t V, double w_H, double w_m,
+                              double w_p, float* confidence, void* stream);
+
 /* Human-readable text of a status code. */
 const char* confkv_status_string(int status);
 

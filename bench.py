@@ -206,6 +206,18 @@ def run_reference(args):
     return 0
 
 
+def reduce_timing(ms: float, steps: int, world_size: int, device):
+    """Max of the per-rank timed milliseconds over all ranks, and the
+    whole-job rate: every rank ran `steps` steps of its own replica."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if world_size > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms_max = float(t.item())
+    return ms_max, world_size * steps / (ms_max / 1000.0)
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -264,11 +276,7 @@ def run_ours(args):
     cache.profile_disable()
     st1 = cache.stats()
 
-    t = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if ws > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    ms_max = float(t.item())
-    steps_per_s = ws * args.steps / (ms_max / 1000.0)
+    ms_max, steps_per_s = reduce_timing(ms, args.steps, ws, dev)
 
     attn_bytes = (st1["attn_bytes"] - st0["attn_bytes"]) / args.steps
     step_bytes = (st1["step_bytes"] - st0["step_bytes"]) / args.steps

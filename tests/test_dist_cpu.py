@@ -1,0 +1,51 @@
+"""The multi-rank logic of bench.py on CPU with gloo, world size 2: each rank
+runs an independent replica; the timing is the max over ranks and the value
+is the whole-job rate.  The reference arm does its work on rank 0 only."""
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, port, results):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE="2")
+    dist.init_process_group("gloo", rank=rank, world_size=2)
+    ms = 100.0 if rank == 0 else 250.0
+    ms_max, value = bench.reduce_timing(ms, 50, 2, torch.device("cpu"))
+    results[rank] = (ms_max, value)
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_timing_is_max_over_ranks_and_value_is_whole_job():
+    port = _free_port()
+    mgr = mp.get_context("spawn").Manager()
+    results = mgr.dict()
+    mp.start_processes(_worker, args=(port, results), nprocs=2, start_method="spawn", join=True)
+    for rank in (0, 1):
+        ms_max, value = results[rank]
+        assert ms_max == 250.0
+        assert abs(value - 2 * 50 / 0.25) < 1e-9
+
+
+def test_single_rank_needs_no_process_group():
+    ms_max, value = bench.reduce_timing(40.0, 20, 1, torch.device("cpu"))
+    assert ms_max == 40.0 and abs(value - 500.0) < 1e-9
+
+
+def test_reference_arm_does_no_work_off_rank_zero(monkeypatch, capsys):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    assert bench.main(["--impl", "reference", "--steps", "3", "--warmup", "3"]) == 0
+    assert capsys.readouterr().out == ""

@@ -1,0 +1,89 @@
+"""Parity at the full workload sizes, in the launch configuration bench.py
+times (the whole batch runs on the GPU).  The oracle cannot follow every
+(sequence, layer) unit, so it regenerates a seeded sample of units from
+their own input streams and follows them step by step: attention output,
+budget, evicted positions and, at the end, the whole cache state of each
+sampled unit.  Units evolve independently given their sequence's confidence,
+so a sample checks the same arithmetic as the full batch.
+
+An eviction decided by a near-tie (oracle scores within 1e-5 of the cut) or a
+budget with |c - tau| < 1e-6 may legitimately differ; the unit is then checked
+for validity and the GPU copy of that unit is replaced by the oracle's state
+(inputs only ever flow from the oracle to the GPU)."""
+import numpy as np
+import pytest
+import torch
+
+import confidence_gated_kv_gb300 as ck
+from oracle import confkv_oracle as orc
+from workload import get_workload, prefill_batch, prefill_unit, step_logits, step_pool, step_unit
+
+from _parity import OUT_TOL, TAU_BAND, check_evictions, compare_unit, unit_to_host
+
+pytestmark = pytest.mark.gpu
+
+
+def _sampled_fullsize(name, seed, steps, n_units, expect_splits=None):
+    w = get_workload(name)
+    prm = orc.Params.from_workload(w)
+    k, v = prefill_batch(w, seed, "cpu")
+    cache = ck.Cache(ck.config_from_workload(w))
+    cache.prefill(k.cuda(), v.cuda(), [w.T0] * w.B)
+    del k, v
+    splits, _ = cache.attention_plan()
+    if expect_splits is not None:
+        assert expect_splits(splits), "launch shape %d CTAs per unit" % splits
+    rng = np.random.default_rng(seed)
+    units = sorted({(int(rng.integers(w.B)), int(rng.integers(w.L))) for _ in range(n_units)})
+    states = {}
+    for b, l in units:
+        kk, vv = prefill_unit(w, seed, b, l)
+        states[(b, l)] = orc.prefill_unit(kk, vv, w.W)
+    q, kn, vn, lg = step_pool(w, seed, steps, "cpu")
+    flagged = 0
+    for s in range(steps):
+        o = cache.step(q[s].cuda(), kn[s].cuda(), vn[s].cuda(), lg[s].cuda())
+        torch.cuda.synchronize()
+        out = o["out"].cpu().numpy()
+        bud = o["budget"].cpu().numpy()
+        nev = o["n_evicted"].cpu().numpy()
+        ev = o["evicted"].cpu().numpy()
+        t = w.T0 + s
+        for b, l in units:
+            c = orc.confidence(step_logits(w, seed, s, b)).c
+            N = orc.budget(c, w.tau, w.n_high[l], w.n_low[l])
+            qq, kk, vv = step_unit(w, seed, s, b, l)
+            r = orc.step_unit(prm, states[(b, l)], t, qq.float().numpy(), kk, vv, N)
+            states[(b, l)] = r.state
+            where = "%s step %d b%d l%d" % (name, s, b, l)
+            err = float(np.abs(out[l, b] - r.o).max())
+            assert err <= OUT_TOL, "%s: attention error %.3g" % (where, err)
+            same = bud[b, l] == N
+            if not same:
+                assert abs(c - w.tau) < TAU_BAND, where + ": budget differs"
+            else:
+                assert nev[l, b] == r.k, "%s: evicted %d vs %d" % (where, nev[l, b], r.k)
+                if r.k:
+                    same = check_evictions(ev[l, b, :r.k], r, where)
+            if not same:
+                flagged += 1
+                cache.import_unit(b, l, unit_to_host(r.state))
+    for b, l in units:
+        compare_unit(cache.export_unit(b, l), states[(b, l)], "%s final b%d l%d" % (name, b, l))
+    assert cache.stats()["device_status"] == 0
+    return flagged
+
+
+def test_qwen32b_shape_sampled_units():
+    # first step evicts 4096 -> 2048 per unit (radix select + sort), then steady state
+    _sampled_fullsize("qwen32b", 4003, steps=3, n_units=5, expect_splits=lambda sp: sp == 1)
+
+
+def test_qwen14b_shape_sampled_units():
+    _sampled_fullsize("qwen14b", 4002, steps=3, n_units=4, expect_splits=lambda sp: sp == 1)
+
+
+def test_needle32k_first_steps_split_path():
+    # 32768-token prefill, first step evicts ~28.7K entries per unit through
+    # the split-K cluster kernel
+    _sampled_fullsize("needle32k", 4004, steps=2, n_units=3, expect_splits=lambda sp: sp > 1)

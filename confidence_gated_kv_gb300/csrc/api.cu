@@ -105,6 +105,7 @@ size_t layout(const Shape& s, char* base, Dev* d, Staging* st) {
   dd.n_high = cv.take<int32_t>(s.L);
   dd.n_low = cv.take<int32_t>(s.L);
   dd.conf = cv.take<ConfPartial>((size_t)s.B * s.SV);
+  dd.cval = cv.take<double>(s.B);
   dd.scratch = cv.take<uint32_t>(lbs * s.S);
   dd.stats = cv.take<DevStats>(1);
   dd.status = cv.take<int32_t>(1);
@@ -286,10 +287,10 @@ int confkv_step(confkv_ctx* ctx, const void* q, const void* k_new, const void* v
   if (prof) cudaEventRecord(ev[0], st);
   if (launch_prestep(s, ctx->d, ctx->steps, logits, k_new, v_new, st) != 0) return CONFKV_ECUDA;
   if (prof) cudaEventRecord(ev[1], st);
-  if (launch_attention(s, ctx->d, q, out, splits, max_tokens, st) != 0) return CONFKV_ECUDA;
+  if (launch_attention(s, ctx->d, q, out, budget, confidence, splits, max_tokens, st) != 0)
+    return CONFKV_ECUDA;
   if (prof) cudaEventRecord(ev[2], st);
-  if (launch_select(s, ctx->d, ctx->steps, budget, confidence, evicted_pos, n_evicted,
-                    (int)k_bound, st) != 0)
+  if (launch_select(s, ctx->d, ctx->steps, evicted_pos, n_evicted, (int)k_bound, st) != 0)
     return CONFKV_ECUDA;
   if (prof) {
     cudaEventRecord(ev[3], st);

@@ -40,7 +40,7 @@
 #include <cuda_bf16.h>
 #include <cooperative_groups.h>
 #include <cfloat>
-#include "confkv_internal.cuh"
+#include "confidence_merge.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -422,6 +422,8 @@ template <int D>
 __global__ void __launch_bounds__(kAttnThreads) attention_kernel(Shape s, Dev d,
                                                                  const void* __restrict__ q,
                                                                  float* __restrict__ out,
+                                                                 int32_t* __restrict__ budget,
+                                                                 float* __restrict__ conf_out,
                                                                  int splits, int chunk_blocks,
                                                                  int stages) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -613,6 +615,8 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(Shape s, Dev d,
     }
   }
   cluster.sync();   // peers keep their shared memory alive until rank 0 has read it
+  // confidence and budgets of sequence blockIdx.x (once per sequence)
+  if ((int)blockIdx.x < s.B && warp == 0) conf_merge_warp(s, d, blockIdx.x, budget, conf_out);
 }
 
 // ===========================================================================
@@ -720,7 +724,8 @@ struct RingPos {
 
 template <int D>
 __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
-    Shape s, Dev d, const void* __restrict__ q, float* __restrict__ out, int stages) {
+    Shape s, Dev d, const void* __restrict__ q, float* __restrict__ out,
+    int32_t* __restrict__ budget, float* __restrict__ conf_out, int stages) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   constexpr int kStageBytes = 128 * D;
   constexpr int kHalf = kStageBytes / 2;
@@ -830,6 +835,9 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
 
   if (warp == kPConsumers + 1) {
     // ------------------------------------------------ epilogue warp
+    // Idle until the first unit is done: merge the confidence of the
+    // sequences this CTA owns (the prestep kernel wrote their partials).
+    for (int b = blockIdx.x; b < s.B; b += gridDim.x) conf_merge_warp(s, d, b, budget, conf_out);
     int k = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++k) {
       const int ps = k & 1;
@@ -1066,8 +1074,8 @@ static int num_sms() {
 int attention_persistent_ctas() { return 2 * num_sms(); }
 
 template <int D>
-static int launch_d(const Shape& s, const Dev& d, const void* q, float* out, int splits,
-                    int max_tokens, cudaStream_t stream) {
+static int launch_d(const Shape& s, const Dev& d, const void* q, float* out, int32_t* budget,
+                    float* conf_out, int splits, int max_tokens, cudaStream_t stream) {
   const int chunk = chunk_of(splits, max_tokens);
   const int smem = attention_smem_bytes(s, splits, max_tokens);
   if (smem > attention_max_smem()) return -1;
@@ -1084,7 +1092,7 @@ static int launch_d(const Shape& s, const Dev& d, const void* q, float* out, int
     int grid = units < 2 * num_sms() ? units : 2 * num_sms();
     if (grid > d.score_ctas) grid = d.score_ctas;
     attention_persistent_kernel<D><<<grid, kPThreads, smem, stream>>>(
-        s, d, q, out, stages_persistent(s));
+        s, d, q, out, budget, conf_out, stages_persistent(s));
     return cudaGetLastError() == cudaSuccess ? 0 : -1;
   }
   static bool configured_split = false;
@@ -1106,15 +1114,15 @@ static int launch_d(const Shape& s, const Dev& d, const void* q, float* out, int
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, attention_kernel<D>, s, d, q, out, splits, chunk,
-                                     stages_split(s, splits, max_tokens));
+  cudaError_t e = cudaLaunchKernelEx(&cfg, attention_kernel<D>, s, d, q, out, budget, conf_out,
+                                     splits, chunk, stages_split(s, splits, max_tokens));
   return e == cudaSuccess ? 0 : -1;
 }
 
-int launch_attention(const Shape& s, const Dev& d, const void* q, float* out, int splits,
-                     int max_tokens, cudaStream_t stream) {
-  if (s.D == 128) return launch_d<128>(s, d, q, out, splits, max_tokens, stream);
-  if (s.D == 64) return launch_d<64>(s, d, q, out, splits, max_tokens, stream);
+int launch_attention(const Shape& s, const Dev& d, const void* q, float* out, int32_t* budget,
+                     float* conf_out, int splits, int max_tokens, cudaStream_t stream) {
+  if (s.D == 128) return launch_d<128>(s, d, q, out, budget, conf_out, splits, max_tokens, stream);
+  if (s.D == 64) return launch_d<64>(s, d, q, out, budget, conf_out, splits, max_tokens, stream);
   return -1;
 }
 

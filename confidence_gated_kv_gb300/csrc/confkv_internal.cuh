@@ -116,6 +116,7 @@ struct Dev {
   int32_t* T0;                     // [b]
   int32_t* n_high; int32_t* n_low; // [l]
   ConfPartial* conf;               // [b][SV]
+  double* cval;                    // [b] confidence of the current step
   uint32_t* scratch;               // [l][b][S] selection keys / compaction pairs
   DevStats* stats;
   int32_t* status;                 // device status word (0 = ok)
@@ -147,10 +148,10 @@ int launch_prefill(const Shape& s, const Dev& d, const void* k, const void* v, l
                    const int32_t* T0_host, cudaStream_t stream);
 int launch_prestep(const Shape& s, const Dev& d, long long step, const float* logits,
                    const void* k_new, const void* v_new, cudaStream_t stream);
-int launch_attention(const Shape& s, const Dev& d, const void* q, float* out, int splits,
-                     int max_tokens, cudaStream_t stream);
-int launch_select(const Shape& s, const Dev& d, long long step, int32_t* budget, float* conf_out,
-                  int32_t* evicted_pos, int32_t* n_evicted, int k_bound, cudaStream_t stream);
+int launch_attention(const Shape& s, const Dev& d, const void* q, float* out, int32_t* budget,
+                     float* conf_out, int splits, int max_tokens, cudaStream_t stream);
+int launch_select(const Shape& s, const Dev& d, long long step, int32_t* evicted_pos,
+                  int32_t* n_evicted, int k_bound, cudaStream_t stream);
 int attention_smem_bytes(const Shape& s, int splits, int max_tokens);
 int attention_max_smem();
 int attention_persistent_ctas();   // persistent CTAs per launch (2 per SM)

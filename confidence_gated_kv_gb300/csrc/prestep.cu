@@ -8,8 +8,9 @@
 // pass gives everything: with M = max z, S = sum exp(z - M) and
 // T = sum (z - M) exp(z - M), the entropy is H = log S - T / S, p(1) = 1 / S
 // and log p(1) - log p(2) = z(1) - z(2).  Each block reduces one chunk of the
-// vocabulary of one sequence to (M, S, T, z(1), z(2)); the select kernel
-// merges the chunks of a sequence in float64.
+// vocabulary of one sequence to (M, S, T, z(1), z(2)); the chunks of a
+// sequence are merged in float64 by one warp of the attention kernel, off its
+// critical path (confidence_merge.cuh).
 //
 // (b) Algorithm 1 step 13 appends the new K/V in FP16.  The ring has W + 16
 // slots, so slot t mod (W + 16) is always free when token t arrives (its
@@ -17,27 +18,12 @@
 // the attention kernel reads the new token as an ordinary ring entry.
 #include <cuda_runtime.h>
 #include <cfloat>
-#include "confkv_internal.cuh"
+#include "confidence_merge.cuh"
 
 namespace confkv {
 
 constexpr int kConfThreads = 256;
 constexpr int kConfPerThread = 16;   // chunk <= 4096 logits
-
-struct Top2 {
-  float z1, z2;
-  int i1;
-};
-
-__device__ __forceinline__ Top2 top2_merge(Top2 a, Top2 b) {
-  Top2 r;
-  if (a.z1 > b.z1 || (a.z1 == b.z1 && a.i1 < b.i1)) {
-    r.z1 = a.z1; r.i1 = a.i1; r.z2 = fmaxf(a.z2, b.z1);
-  } else {
-    r.z1 = b.z1; r.i1 = b.i1; r.z2 = fmaxf(b.z2, a.z1);
-  }
-  return r;
-}
 
 __device__ void conf_block(const Shape& s, const Dev& d, const float* __restrict__ logits, int b,
                            int part) {

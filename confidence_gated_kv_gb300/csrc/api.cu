@@ -71,6 +71,7 @@ Shape make_shape(const confkv_config* c) {
   s.WR = (int)align_up(c->W + kRingExtra, 16);
   s.P = c->P;
   s.S = s.cap + s.WR;
+  s.cstride = s.cap + 16;
   // vocabulary chunks per sequence: <= 4096 logits each, and enough blocks
   // in total to cover the GPU a few times over
   const int min_sv = (c->V + 4095) / 4096;
@@ -91,8 +92,8 @@ size_t layout(const Shape& s, char* base, Dev* d, Staging* st) {
   const size_t units = (size_t)s.L * s.B * s.Hkv;
   const size_t lbs = (size_t)s.L * s.B;
   Dev dd{};
-  dd.k8 = cv.take<uint8_t>(units * s.cap * s.D);
-  dd.v8 = cv.take<uint8_t>(units * s.cap * s.D);
+  dd.k8 = cv.take<uint8_t>(units * s.cstride * s.D);
+  dd.v8 = cv.take<uint8_t>(units * s.cstride * s.D);
   dd.k16 = cv.take<__half>(units * s.WR * s.D);
   dd.v16 = cv.take<__half>(units * s.WR * s.D);
   dd.sK = cv.take<float>(units * s.D);
@@ -341,7 +342,7 @@ static int copy_unit_raw(confkv_ctx* ctx, int b, int l, std::vector<uint8_t>& k8
                          cudaStream_t st) {
   const Shape& s = ctx->s;
   const int D = s.D;
-  k8.resize((size_t)s.Hkv * s.cap * D);
+  k8.resize((size_t)s.Hkv * s.cstride * D);
   v8.resize(k8.size());
   k16.resize((size_t)s.Hkv * s.WR * D);
   v16.resize(k16.size());
@@ -350,8 +351,8 @@ static int copy_unit_raw(confkv_ctx* ctx, int b, int l, std::vector<uint8_t>& k8
   sK.resize((size_t)s.Hkv * D);
   sV.resize(sK.size());
   const size_t u0 = unit_index(s, l, b, 0), lb = lb_index(s, l, b);
-  cudaError_t e = cudaMemcpyAsync(k8.data(), ctx->d.k8 + u0 * s.cap * D, k8.size(), cudaMemcpyDeviceToHost, st);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(v8.data(), ctx->d.v8 + u0 * s.cap * D, v8.size(), cudaMemcpyDeviceToHost, st);
+  cudaError_t e = cudaMemcpyAsync(k8.data(), ctx->d.k8 + u0 * s.cstride * D, k8.size(), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(v8.data(), ctx->d.v8 + u0 * s.cstride * D, v8.size(), cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(k16.data(), ctx->d.k16 + u0 * s.WR * D, k16.size() * 2, cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(v16.data(), ctx->d.v16 + u0 * s.WR * D, v16.size() * 2, cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(pos.data(), ctx->d.pos + lb * s.S, s.S * 4, cudaMemcpyDeviceToHost, st);
@@ -382,7 +383,7 @@ int confkv_export_unit(confkv_ctx* ctx, int32_t b, int32_t l, confkv_unit_host* 
     o->pos8[i] = pos[i];
     o->ema8[i] = ema[i];
     for (int h = 0; h < Hkv; ++h) {
-      const size_t blk = ((size_t)h * s.cap + (i & ~15)) * D;
+      const size_t blk = ((size_t)h * s.cstride + (i & ~15)) * D;
       for (int c = 0; c < D; ++c) {
         o->k8[((size_t)i * Hkv + h) * D + c] = (int8_t)((int)k8[blk + k8_offset(D, i & 15, c)] - kCodeBias);
         o->v8[((size_t)i * Hkv + h) * D + c] = (int8_t)((int)v8[blk + v8_offset(D, i & 15, c)] - kCodeBias);
@@ -421,7 +422,7 @@ int confkv_import_unit(confkv_ctx* ctx, int32_t b, int32_t l, const confkv_unit_
   if ((in->n8 && (!in->pos8 || !in->ema8 || !in->k8 || !in->v8)) ||
       (in->nR && (!in->posR || !in->emaR || !in->k16 || !in->v16)) || !in->sK || !in->sV)
     return CONFKV_EINVAL;
-  std::vector<uint8_t> k8((size_t)Hkv * s.cap * D, kCodeBias), v8(k8.size(), kCodeBias);
+  std::vector<uint8_t> k8((size_t)Hkv * s.cstride * D, kCodeBias), v8(k8.size(), kCodeBias);
   std::vector<uint16_t> k16((size_t)Hkv * s.WR * D, 0), v16(k16.size(), 0);
   std::vector<int32_t> pos(s.S, -1);
   std::vector<float> ema(s.S, 0.f);
@@ -430,7 +431,7 @@ int confkv_import_unit(confkv_ctx* ctx, int32_t b, int32_t l, const confkv_unit_
     pos[i] = in->pos8[i];
     ema[i] = in->ema8[i];
     for (int h = 0; h < Hkv; ++h) {
-      const size_t blk = ((size_t)h * s.cap + (i & ~15)) * D;
+      const size_t blk = ((size_t)h * s.cstride + (i & ~15)) * D;
       for (int c = 0; c < D; ++c) {
         const int ck = in->k8[((size_t)i * Hkv + h) * D + c], cv = in->v8[((size_t)i * Hkv + h) * D + c];
         if (ck < -127 || cv < -127) return CONFKV_EINVAL;   // codes are symmetric
@@ -457,8 +458,8 @@ int confkv_import_unit(confkv_ctx* ctx, int32_t b, int32_t l, const confkv_unit_
   cudaStream_t st = as_stream(stream);
   const size_t u0 = unit_index(s, l, b, 0), lb = lb_index(s, l, b);
   int32_t n8 = in->n8;
-  cudaError_t e = cudaMemcpyAsync(ctx->d.k8 + u0 * s.cap * D, k8.data(), k8.size(), cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->d.v8 + u0 * s.cap * D, v8.data(), v8.size(), cudaMemcpyHostToDevice, st);
+  cudaError_t e = cudaMemcpyAsync(ctx->d.k8 + u0 * s.cstride * D, k8.data(), k8.size(), cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->d.v8 + u0 * s.cstride * D, v8.data(), v8.size(), cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->d.k16 + u0 * s.WR * D, k16.data(), k16.size() * 2, cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->d.v16 + u0 * s.WR * D, v16.data(), v16.size() * 2, cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(ctx->d.pos + lb * s.S, pos.data(), s.S * 4, cudaMemcpyHostToDevice, st);

@@ -465,8 +465,8 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(Shape s, Dev d,
   const size_t qoff = (lb * s.Hq + (size_t)h * G) * D;
   const float* sKu = d.sK + (size_t)u * D;
   const float* sVu = d.sV + (size_t)u * D;
-  const uint8_t* k8u = d.k8 + (size_t)u * s.cap * D;
-  const uint8_t* v8u = d.v8 + (size_t)u * s.cap * D;
+  const uint8_t* k8u = d.k8 + (size_t)u * s.cstride * D;
+  const uint8_t* v8u = d.v8 + (size_t)u * s.cstride * D;
   const char* k16u = reinterpret_cast<const char*>(d.k16) + (size_t)u * s.WR * D * 2;
   const char* v16u = reinterpret_cast<const char*>(d.v16) + (size_t)u * s.WR * D * 2;
   const int32_t* posR = d.pos + lb * s.S + s.cap;
@@ -799,8 +799,8 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
         // K/V stages
         Sched sch;
         sch.init(0, nb8 + nbR, nb8);
-        const char* k8u = reinterpret_cast<const char*>(d.k8) + (size_t)u * s.cap * D;
-        const char* v8u = reinterpret_cast<const char*>(d.v8) + (size_t)u * s.cap * D;
+        const char* k8u = reinterpret_cast<const char*>(d.k8) + (size_t)u * s.cstride * D;
+        const char* v8u = reinterpret_cast<const char*>(d.v8) + (size_t)u * s.cstride * D;
         const char* k16u = reinterpret_cast<const char*>(d.k16) + (size_t)u * s.WR * D * 2;
         const char* v16u = reinterpret_cast<const char*>(d.v16) + (size_t)u * s.WR * D * 2;
         bool ok = true;

@@ -11,7 +11,8 @@
 //   Attention-mass partials [l][b][kvh][S] (fp32, one per KV head).
 //
 //   K/V payload per unit u = (l, b, kvh), in 16-token blocks:
-//     INT8:  k8, v8  [u][cap/16][16*D bytes], each byte the code + 128
+//     INT8:  k8, v8  [u][cstride/16][16*D bytes], each byte the code + 128;
+//                    cstride = cap + 16 slots (only the first cap are used)
 //                    (code in [-127, 127], stored biased as uint8)
 //     FP16:  k16,v16 [u][WR/16][16*D halves]
 //   Inside a block the bytes are interleaved so that lane `lane` of a warp
@@ -99,6 +100,8 @@ struct DevStats {        // cumulative counters, updated with atomics
 struct Shape {
   int L, B, Hq, Hkv, G, D, V;
   int cap, W, WR, P, S;      // S = cap + WR slots per (l, b)
+  int cstride;               // INT8 slots between consecutive units in memory (cap + 16):
+                             // unit bases do not all share one power-of-two alignment
   int SV;                    // confidence partial blocks per sequence
   int qbf16;                 // query dtype: 0 fp16, 1 bf16
   int max_evict;             // rows of evicted_pos per (l, b)

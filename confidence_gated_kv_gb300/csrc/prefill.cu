@@ -77,7 +77,7 @@ __global__ void prefill_place_kernel(Shape s, Dev d, const __half* __restrict__ 
     if (p < n8) {
       const float sk = scale_from_absmax(d.absmax[(size_t)u * D + c]);
       const float sv = scale_from_absmax(d.absmax[nu + (size_t)u * D + c]);
-      const size_t blk_base = ((size_t)u * (s.cap / 16) + (p >> 4)) * 16 * D;
+      const size_t blk_base = ((size_t)u * (s.cstride / 16) + (p >> 4)) * 16 * D;
       d.k8[blk_base + k8_offset(D, p & 15, c)] = quant_code(xk, sk);
       d.v8[blk_base + v8_offset(D, p & 15, c)] = quant_code(xv, sv);
       if (h == 0 && c == 0) {
@@ -110,8 +110,8 @@ int launch_prefill(const Shape& s, const Dev& d, const void* k, const void* v, l
   cudaMemsetAsync(d.ema, 0, (size_t)s.L * s.B * s.S * sizeof(float), stream);
   cudaMemsetAsync(d.k16, 0, units * s.WR * s.D * sizeof(__half), stream);
   cudaMemsetAsync(d.v16, 0, units * s.WR * s.D * sizeof(__half), stream);
-  cudaMemsetAsync(d.k8, kCodeBias, units * (size_t)s.cap * s.D, stream);
-  cudaMemsetAsync(d.v8, kCodeBias, units * (size_t)s.cap * s.D, stream);
+  cudaMemsetAsync(d.k8, kCodeBias, units * (size_t)s.cstride * s.D, stream);
+  cudaMemsetAsync(d.v8, kCodeBias, units * (size_t)s.cstride * s.D, stream);
   // Sequences with T0 = 0 still need their scales (1.0) and n8 = 0.
   int tsplit = tmax0 > 0 ? (tmax0 + 1023) / 1024 : 1;
   if (tsplit > 64) tsplit = 64;

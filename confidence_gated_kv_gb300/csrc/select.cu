@@ -363,8 +363,8 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(Shape s, Dev d, 
       for (int i = threadIdx.x; do_move && i < s.Hkv * per_tok; i += kSelThreads) {
         const int h = i / per_tok, e = i % per_tok;
         const size_t u = unit_index(s, l, b, h);
-        uint8_t* k8u = d.k8 + u * (size_t)s.cap * D;
-        uint8_t* v8u = d.v8 + u * (size_t)s.cap * D;
+        uint8_t* k8u = d.k8 + u * (size_t)s.cstride * D;
+        uint8_t* v8u = d.v8 + u * (size_t)s.cstride * D;
         if (e < D / 4) {
           const int c0 = (e / 4) * 16 + 2 * (e % 4);
           *reinterpret_cast<uint32_t*>(k8u + (size_t)(dst >> 4) * 16 * D + k8_offset(D, dst & 15, c0)) =
@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(Shape s, Dev d, 
         const size_t rblk = (u * (s.WR / 16) + (rs >> 4)) * 16 * D * 2;
         const float xk = __half2float(*reinterpret_cast<const __half*>(k16b + rblk + k16_offset(D, rs & 15, c)));
         const float xv = __half2float(*reinterpret_cast<const __half*>(v16b + rblk + v16_offset(D, rs & 15, c)));
-        const size_t dblk = (u * (size_t)(s.cap / 16) + (n8p >> 4)) * 16 * D;
+        const size_t dblk = (u * (size_t)(s.cstride / 16) + (n8p >> 4)) * 16 * D;
         d.k8[dblk + k8_offset(D, n8p & 15, c)] = quant_code_sel(xk, d.sK[u * D + c]);
         d.v8[dblk + v8_offset(D, n8p & 15, c)] = quant_code_sel(xv, d.sV[u * D + c]);
       }
@@ -406,8 +406,8 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(Shape s, Dev d, 
       if (do_move && i < s.Hkv * per_tok) {
         const int h = i / per_tok, e = i % per_tok;
         const size_t u = unit_index(s, l, b, h);
-        const uint8_t* k8u = d.k8 + u * (size_t)s.cap * D;
-        const uint8_t* v8u = d.v8 + u * (size_t)s.cap * D;
+        const uint8_t* k8u = d.k8 + u * (size_t)s.cstride * D;
+        const uint8_t* v8u = d.v8 + u * (size_t)s.cstride * D;
         mv[j] = e < D / 4 ? *reinterpret_cast<const uint32_t*>(
                                 k8u + (size_t)(src >> 4) * 16 * D +
                                 k8_offset(D, src & 15, (e / 4) * 16 + 2 * (e % 4)))
@@ -444,8 +444,8 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(Shape s, Dev d, 
       if (do_move && i < s.Hkv * per_tok) {
         const int h = i / per_tok, e = i % per_tok;
         const size_t u = unit_index(s, l, b, h);
-        uint8_t* k8u = d.k8 + u * (size_t)s.cap * D;
-        uint8_t* v8u = d.v8 + u * (size_t)s.cap * D;
+        uint8_t* k8u = d.k8 + u * (size_t)s.cstride * D;
+        uint8_t* v8u = d.v8 + u * (size_t)s.cstride * D;
         if (e < D / 4)
           *reinterpret_cast<uint32_t*>(k8u + (size_t)(dst >> 4) * 16 * D +
                                        k8_offset(D, dst & 15, (e / 4) * 16 + 2 * (e % 4))) = mv[j];
@@ -459,7 +459,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(Shape s, Dev d, 
       if (do_req && i < s.Hkv * D) {
         const int h = i / D, c = i % D;
         const size_t u = unit_index(s, l, b, h);
-        const size_t dblk = (u * (size_t)(s.cap / 16) + (n8p >> 4)) * 16 * D;
+        const size_t dblk = (u * (size_t)(s.cstride / 16) + (n8p >> 4)) * 16 * D;
         d.k8[dblk + k8_offset(D, n8p & 15, c)] = quant_code_sel(xk[j], sk[j]);
         d.v8[dblk + v8_offset(D, n8p & 15, c)] = quant_code_sel(xv[j], sv[j]);
       }
@@ -521,8 +521,8 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(Shape s, Dev d, 
         const int h = rest / per_tok, e = rest % per_tok;
         const int src = (int)mover[r], dst = (int)hole[r];
         const size_t u = unit_index(s, l, b, h);
-        uint8_t* k8u = d.k8 + u * (size_t)s.cap * D;
-        uint8_t* v8u = d.v8 + u * (size_t)s.cap * D;
+        uint8_t* k8u = d.k8 + u * (size_t)s.cstride * D;
+        uint8_t* v8u = d.v8 + u * (size_t)s.cstride * D;
         if (e < D / 4) {
           // one 32-bit word = channels {16kk+2t, +1, +8, +9} of the token
           const int c0 = (e / 4) * 16 + 2 * (e % 4);
@@ -551,7 +551,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(Shape s, Dev d, 
         const size_t rblk = (u * (s.WR / 16) + (rs >> 4)) * 16 * D * 2;
         const float xk = __half2float(*reinterpret_cast<const __half*>(k16b + rblk + k16_offset(D, rs & 15, c)));
         const float xv = __half2float(*reinterpret_cast<const __half*>(v16b + rblk + v16_offset(D, rs & 15, c)));
-        const size_t dblk = (u * (size_t)(s.cap / 16) + (n8p >> 4)) * 16 * D;
+        const size_t dblk = (u * (size_t)(s.cstride / 16) + (n8p >> 4)) * 16 * D;
         d.k8[dblk + k8_offset(D, n8p & 15, c)] = quant_code_sel(xk, d.sK[u * D + c]);
         d.v8[dblk + v8_offset(D, n8p & 15, c)] = quant_code_sel(xv, d.sV[u * D + c]);
       }

@@ -102,23 +102,21 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(Shape s, Dev d, 
   {
     // The first kCache slots of this thread: every load is issued before any
     // value is used (positions, then the KV-head mass partials and the EMA).
-#pragma unroll
-    for (int c = 0; c < kCache; ++c) {
-      const int i = threadIdx.x + c * kSelThreads;
-      const int slot = i < n8 ? i : s.cap + (i - n8);
-      cpos[c] = i < nvirt ? pos[slot] : -1;
-    }
+    // positions, EMA and the KV-head mass partials are all loaded in one
+    // round (slots that turn out to be empty simply ignore their values)
     float A[kCache], eold[kCache];
 #pragma unroll
     for (int c = 0; c < kCache; ++c) {
       const int i = threadIdx.x + c * kSelThreads;
       const int slot = i < n8 ? i : s.cap + (i - n8);
+      cpos[c] = -1;
       A[c] = 0.f;
       eold[c] = 0.f;
-      if (i < nvirt && cpos[c] >= 0) {
+      if (i < nvirt) {
+        cpos[c] = pos[slot];
+        eold[c] = ema[slot];
         const float* mp = d.mass + lb * s.Hkv * s.S + slot;
         for (int h = 0; h < s.Hkv; ++h) A[c] += __ldg(mp + (size_t)h * s.S);
-        eold[c] = ema[slot];
       }
     }
 #pragma unroll
@@ -397,8 +395,10 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(Shape s, Dev d, 
       __syncthreads();
       if (threadIdx.x == 0 && do_req) { pos[n8p] = tl; ema[n8p] = rema; pos[rslot] = -1; }
     } else {
+    // every load of this phase is issued before any value is used
     uint32_t mv[kMv];
-    float xk[kRq], xv[kRq], sk[kRq], sv[kRq];
+    unsigned short xk[kRq], xv[kRq];
+    float sk[kRq], sv[kRq];
 #pragma unroll
     for (int j = 0; j < kMv; ++j) {
       const int i = threadIdx.x + j * kSelThreads;
@@ -408,10 +408,11 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(Shape s, Dev d, 
         const size_t u = unit_index(s, l, b, h);
         const uint8_t* k8u = d.k8 + u * (size_t)s.cstride * D;
         const uint8_t* v8u = d.v8 + u * (size_t)s.cstride * D;
-        mv[j] = e < D / 4 ? *reinterpret_cast<const uint32_t*>(
-                                k8u + (size_t)(src >> 4) * 16 * D +
-                                k8_offset(D, src & 15, (e / 4) * 16 + 2 * (e % 4)))
-                          : v8u[(size_t)(src >> 4) * 16 * D + v8_offset(D, src & 15, e - D / 4)];
+        if (e < D / 4)
+          mv[j] = *reinterpret_cast<const uint32_t*>(k8u + (size_t)(src >> 4) * 16 * D +
+                                                     k8_offset(D, src & 15, (e / 4) * 16 + 2 * (e % 4)));
+        else
+          mv[j] = v8u[(size_t)(src >> 4) * 16 * D + v8_offset(D, src & 15, e - D / 4)];
       }
     }
     const char* k16b = reinterpret_cast<const char*>(d.k16);
@@ -419,14 +420,14 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(Shape s, Dev d, 
 #pragma unroll
     for (int j = 0; j < kRq; ++j) {
       const int i = threadIdx.x + j * kSelThreads;
-      xk[j] = xv[j] = 0.f;
+      xk[j] = xv[j] = 0;
       sk[j] = sv[j] = 1.f;
       if (do_req && i < s.Hkv * D) {
         const int h = i / D, c = i % D;
         const size_t u = unit_index(s, l, b, h);
         const size_t rblk = (u * (s.WR / 16) + (rs >> 4)) * 16 * D * 2;
-        xk[j] = __half2float(*reinterpret_cast<const __half*>(k16b + rblk + k16_offset(D, rs & 15, c)));
-        xv[j] = __half2float(*reinterpret_cast<const __half*>(v16b + rblk + v16_offset(D, rs & 15, c)));
+        xk[j] = *reinterpret_cast<const unsigned short*>(k16b + rblk + k16_offset(D, rs & 15, c));
+        xv[j] = *reinterpret_cast<const unsigned short*>(v16b + rblk + v16_offset(D, rs & 15, c));
         sk[j] = d.sK[u * D + c];
         sv[j] = d.sV[u * D + c];
       }
@@ -460,8 +461,8 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(Shape s, Dev d, 
         const int h = i / D, c = i % D;
         const size_t u = unit_index(s, l, b, h);
         const size_t dblk = (u * (size_t)(s.cstride / 16) + (n8p >> 4)) * 16 * D;
-        d.k8[dblk + k8_offset(D, n8p & 15, c)] = quant_code_sel(xk[j], sk[j]);
-        d.v8[dblk + v8_offset(D, n8p & 15, c)] = quant_code_sel(xv[j], sv[j]);
+        d.k8[dblk + k8_offset(D, n8p & 15, c)] = quant_code_sel(__half2float(__ushort_as_half(xk[j])), sk[j]);
+        d.v8[dblk + v8_offset(D, n8p & 15, c)] = quant_code_sel(__half2float(__ushort_as_half(xv[j])), sv[j]);
       }
     }
     if (threadIdx.x == 0) {

@@ -285,6 +285,16 @@ def run_ours(args):
     achieved = attn_bytes / (attn_ms / 1000.0) / 1e9
     traffic = _traffic_from_profiles("attention_kernel_" + w.name)
 
+    # attention + compaction chain: everything but the logits reduction and the
+    # append of the new token (attention, EMA, ranking, eviction, compaction,
+    # requantisation), over the time of the attention and select kernels
+    prestep_bytes = w.B * w.V * 4 + w.L * w.B * w.Hkv * w.d * 2 * 2 * 2
+    chain_bytes = step_bytes - prestep_bytes
+    chain_ms = (prof["attention_ms"] + prof["select_ms"]) / max(prof["steps"], 1)
+    chain_gbs = chain_bytes / (chain_ms / 1000.0) / 1e9
+    chain = {"what": "attention + EMA/rank/evict/compact/requant", "algorithmic_bytes_per_step": chain_bytes,
+             "ms_per_step": chain_ms, "achieved_gbs": chain_gbs, "peak_gbs": peak, "frac": chain_gbs / peak}
+
     # ------------------------------------------------ end to end, host buffers
     e2e = None
     if args.e2e_steps > 0:
@@ -337,6 +347,7 @@ def run_ours(args):
                          "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                          "traffic": traffic, "algorithmic_bytes_per_launch": attn_bytes,
                          "avg_launch_ms": attn_ms, "peak_kind": peak_kind},
+            "chain": chain,
             "breakdown_ms_per_step": {k: prof[k + "_ms"] / max(prof["steps"], 1)
                                       for k in ("prestep", "attention", "select")},
             "attention_launch": {"ctas_per_unit": splits, "smem_bytes": smem},

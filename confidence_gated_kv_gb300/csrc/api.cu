@@ -291,7 +291,7 @@ int confkv_step(confkv_ctx* ctx, const void* q, const void* k_new, const void* v
   if (launch_attention(s, ctx->d, q, out, budget, confidence, splits, max_tokens, st) != 0)
     return CONFKV_ECUDA;
   if (prof) cudaEventRecord(ev[2], st);
-  if (launch_select(s, ctx->d, ctx->steps, evicted_pos, n_evicted, (int)k_bound, st) != 0)
+  if (launch_select(s, ctx->d, ctx->steps, evicted_pos, n_evicted, st) != 0)
     return CONFKV_ECUDA;
   if (prof) {
     cudaEventRecord(ev[3], st);

@@ -154,7 +154,7 @@ int launch_prestep(const Shape& s, const Dev& d, long long step, const float* lo
 int launch_attention(const Shape& s, const Dev& d, const void* q, float* out, int32_t* budget,
                      float* conf_out, int splits, int max_tokens, cudaStream_t stream);
 int launch_select(const Shape& s, const Dev& d, long long step, int32_t* evicted_pos,
-                  int32_t* n_evicted, int k_bound, cudaStream_t stream);
+                  int32_t* n_evicted, cudaStream_t stream);
 int attention_smem_bytes(const Shape& s, int splits, int max_tokens);
 int attention_max_smem();
 int attention_persistent_ctas();   // persistent CTAs per launch (2 per SM)

@@ -1,5 +1,5 @@
-// Last kernel of a decode step, one CTA per (layer, sequence): confidence and
-// budget, EMA update, ranking, bottom-k selection, evicted-position output,
+// Last kernel of a decode step, one CTA per (layer, sequence): budget, EMA
+// update, ranking, bottom-k selection, the sorted evicted positions,
 // compaction of the INT8 region and requantisation of the token that leaves
 // the FP16 window.
 //
@@ -20,6 +20,19 @@
 // survivors above it (at most k moves), so the region stays dense without
 // an indirection table (gist.science/de/paper/2605.24786, Systemintegration:
 // contiguous compaction).  Evicted FP16 ring slots are just marked empty.
+//
+// Work layout.  The whole CTA walks the slots four at a time (int4 / float4
+// loads of pos, EMA and the KV-head mass partials).  Ranking keys and the
+// candidate positions go to shared memory (global scratch when a cache is too
+// long for it).  One eviction is a block argmin; more use a radix select on
+// the 32-bit keys (8-bit digits), with a second pass over positions only when
+// keys tie exactly at the cut.  The evicted positions come out sorted from a
+// bitmap over the position range.  Token payload work (moves and the
+// requantisation) gives each warp one KV head: lane i owns one 32-bit word
+// of the token's INT8 K (the four channels of one mma fragment) and the V
+// channels i, i + 32, ...; the same lane-to-byte map for a move and the
+// requantisation lets one thread read a slot before it rewrites it, so the
+// common one-eviction path needs no barrier between them.
 #include <cuda_runtime.h>
 #include <cfloat>
 #include <climits>
@@ -29,553 +42,560 @@ namespace confkv {
 
 constexpr int kSelThreads = 256;
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kCache = 6;   // slots per thread kept in registers between passes
+constexpr int kPosWords = 2048;            // sorted-output bitmap: 65536 positions per window
+constexpr uint32_t kNoKey = 0xffffffffu;   // ranking key of a slot that is not a candidate
+constexpr size_t kSelSmemKeysMax = 100 * 1024;
+
+// Byte offsets into the dynamic shared memory of the select kernel.
+struct SelSmem {
+  int off_posbits;   // [kPosWords] u32
+  int off_bm8;       // [cap / 32] u32: evicted INT8 slots
+  int off_key;       // [S] u32 keys, then the compaction lists (keys in shared memory only)
+  int off_pos;       // [S] i32 candidate positions, INT_MAX elsewhere (keys in shared memory only)
+  int bytes;
+};
 
 // Stored byte of code = clamp(rint(x / s), -127, 127): the code + 128.
-__device__ __forceinline__ uint8_t quant_code_sel(float x, float s) {
+__device__ __forceinline__ uint32_t quant_code_sel(float x, float s) {
   float r = rintf(__fdiv_rn(x, s));
   r = fminf(fmaxf(r, -127.f), 127.f);
-  return (uint8_t)((int)r + kCodeBias);
+  return (uint32_t)((int)r + kCodeBias);
 }
 
-template <typename T, typename Op>
-__device__ __forceinline__ T block_reduce(T v, Op op, T* red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Warp 0 scans a 256-bin histogram for the digit that holds the rem-th
+// smallest element; the other threads wait at the caller's barrier.
+__device__ __forceinline__ void hist_find(const int* hist, int rem, int lane, int* s_digit,
+                                          int* s_rem, int* s_dcnt) {
+  int cnt[8], run = 0;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = op(v, __shfl_xor_sync(0xffffffffu, v, o));
-  __syncthreads();
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  T r = red[0];
-  for (int w = 1; w < kSelWarps; ++w) r = op(r, red[w]);
-  return r;
+  for (int j = 0; j < 8; ++j) {
+    cnt[j] = hist[lane * 8 + j];
+    run += cnt[j];
+  }
+  int incl = run;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  int before = incl - run;
+  if (before < rem && rem <= incl) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (before < rem && rem <= before + cnt[j]) {
+        *s_digit = lane * 8 + j;
+        *s_rem = rem - before;
+        *s_dcnt = cnt[j];
+      }
+      before += cnt[j];
+    }
+  }
 }
 
-struct MinOp { template <typename T> __device__ T operator()(T a, T b) const { return a < b ? a : b; } };
-struct MaxOp { template <typename T> __device__ T operator()(T a, T b) const { return a > b ? a : b; } };
-struct AddOp { template <typename T> __device__ T operator()(T a, T b) const { return a + b; } };
-
+template <int D, bool kSmemKeys>
 __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(Shape s, Dev d, long long step,
                                                              int32_t* __restrict__ evicted_out,
                                                              int32_t* __restrict__ nevict_out,
-                                                             int sort_cap) {
-  extern __shared__ __align__(16) uint32_t dsm[];
-  uint32_t* bitmap = dsm;                                  // [cap/32] evicted INT8 slots
-  int32_t* list = reinterpret_cast<int32_t*>(dsm + s.cap / 32);   // [sort_cap]
+                                                             SelSmem sm) {
+  extern __shared__ __align__(16) unsigned char dsm[];
+  uint32_t* posbits = reinterpret_cast<uint32_t*>(dsm + sm.off_posbits);
+  uint32_t* bm8 = reinterpret_cast<uint32_t*>(dsm + sm.off_bm8);
+  __shared__ int red_i[kSelWarps][4];
+  __shared__ float red_f[kSelWarps][2];
   __shared__ unsigned long long red64[kSelWarps];
-  __shared__ int redi[kSelWarps];
   __shared__ int hist[256];
-  __shared__ int red5i[kSelWarps][3];
-  __shared__ float red5f[kSelWarps][2];
-  __shared__ int s_cnt, s_k8, s_digit, s_remaining, s_evslot;
-  __shared__ unsigned long long s_prefix, s_mask;
+  __shared__ int scan_w[kSelWarps];
+  __shared__ int s_digit, s_rem, s_dcnt, s_cnt, s_k8, s_evslot, s_evpos;
 
   const int l = blockIdx.x / s.B, b = blockIdx.x % s.B;
   const size_t lb = lb_index(s, l, b);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int32_t* pos = d.pos + lb * s.S;
-  float* ema = d.ema + lb * s.S;
-  uint32_t* keys = d.scratch + lb * s.S;
+  const int cap = s.cap, WR = s.WR, S = s.S, Hkv = s.Hkv;
+  int32_t* pos = d.pos + lb * S;
+  float* ema = d.ema + lb * S;
+  const float* mass = d.mass + lb * (size_t)Hkv * S;
+  uint32_t* KEY = kSmemKeys ? reinterpret_cast<uint32_t*>(dsm + sm.off_key) : d.scratch + lb * S;
+  int32_t* SPOS = kSmemKeys ? reinterpret_cast<int32_t*>(dsm + sm.off_pos) : nullptr;
   const int t = d.T0[b] + (int)step;
   const int n8 = d.n8[lb];
+  const int thr = t - s.P;                 // candidates: pos < t - P
+  const int tl = t - s.W;                  // position leaving the FP16 window
+  const int rs = tl >= 0 ? tl % WR : 0;
+  const int rslot = cap + rs;
+  const int prs = tl >= 0 ? pos[rslot] : -1;   // read before any slot of this step changes
+  const int nvirt = n8 + WR;               // element e: INT8 slot e < n8, else ring slot cap + e - n8
+  auto slot_of = [&](int e) { return e < n8 ? e : cap + (e - n8); };
+
   if (threadIdx.x == 0) {
     s_cnt = 0;
     s_k8 = 0;
     s_evslot = -1;
+    s_evpos = -1;
   }
+  for (int w = threadIdx.x; w < (n8 + 31) / 32; w += kSelThreads) bm8[w] = 0u;
 
   // ------------------------------------------------ 1. budget of this layer
-  // c was merged once per sequence by the last confidence block of the step.
+  // c was merged once per sequence by the attention kernel of this step.
   const int N = (d.cval[b] >= s.tau) ? d.n_high[l] : d.n_low[l];
 
-  // ------------------------------------------------ 2. EMA update + candidate ranges
-  // Virtual index i < n8: INT8 slot i; otherwise ring slot cap + (i - n8).
-  // The first kCache slots of every thread stay in registers for pass 3.
-  const int nvirt = n8 + s.WR;
-  const int thr = t - s.P;               // candidates: pos < t - P
+  // ------------------------------------------------ 2. EMA update, candidate ranges
+  const int q8 = (n8 + 3) >> 2;            // INT8 quads (the last one may be partial)
+  const int nq = q8 + (WR >> 2);
   const float lam = s.lam, inv_hq = 1.0f / (float)s.Hq;
-  int nring = 0;
+  int nring = 0, ncand = 0;
   float amin = FLT_MAX, amax = -FLT_MAX;
   int pmin = INT_MAX, pmax = INT_MIN;
-  int cpos[kCache];
-  float cema[kCache];
-  {
-    // The first kCache slots of this thread: every load is issued before any
-    // value is used (positions, then the KV-head mass partials and the EMA).
-    // positions, EMA and the KV-head mass partials are all loaded in one
-    // round (slots that turn out to be empty simply ignore their values)
-    float A[kCache], eold[kCache];
+  for (int q0 = threadIdx.x; q0 < nq; q0 += 2 * kSelThreads) {
+    int4 P4[2];
+    float4 E4[2], A4[2];
 #pragma unroll
-    for (int c = 0; c < kCache; ++c) {
-      const int i = threadIdx.x + c * kSelThreads;
-      const int slot = i < n8 ? i : s.cap + (i - n8);
-      cpos[c] = -1;
-      A[c] = 0.f;
-      eold[c] = 0.f;
-      if (i < nvirt) {
-        cpos[c] = pos[slot];
-        eold[c] = ema[slot];
-        const float* mp = d.mass + lb * s.Hkv * s.S + slot;
-        for (int h = 0; h < s.Hkv; ++h) A[c] += __ldg(mp + (size_t)h * s.S);
+    for (int r = 0; r < 2; ++r) {
+      const int q = q0 + r * kSelThreads;
+      P4[r] = make_int4(-1, -1, -1, -1);
+      E4[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+      A4[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (q < nq) {
+        const int slot0 = q < q8 ? 4 * q : cap + 4 * (q - q8);
+        P4[r] = *reinterpret_cast<const int4*>(pos + slot0);
+        E4[r] = *reinterpret_cast<const float4*>(ema + slot0);
       }
     }
+#pragma unroll 4
+    for (int h = 0; h < Hkv; ++h) {
 #pragma unroll
-    for (int c = 0; c < kCache; ++c) {
-      const int i = threadIdx.x + c * kSelThreads;
-      const int p = cpos[c];
-      cema[c] = 0.f;
-      if (i < nvirt && p >= 0) {
-        const int slot = i < n8 ? i : s.cap + (i - n8);
-        nring += (i >= n8);
-        const float a = fmaf(lam, eold[c], (1.0f - lam) * (A[c] * inv_hq));
-        ema[slot] = a;
-        cema[c] = a;
-        if (p < thr) {
-          amin = fminf(amin, a); amax = fmaxf(amax, a);
-          pmin = min(pmin, p); pmax = max(pmax, p);
+      for (int r = 0; r < 2; ++r) {
+        const int q = q0 + r * kSelThreads;
+        if (q < nq) {
+          const int slot0 = q < q8 ? 4 * q : cap + 4 * (q - q8);
+          const float4 m = __ldg(reinterpret_cast<const float4*>(mass + (size_t)h * S + slot0));
+          A4[r].x += m.x; A4[r].y += m.y; A4[r].z += m.z; A4[r].w += m.w;
         }
       }
     }
-    // slots beyond the register cache (long caches)
-    for (int i = threadIdx.x + kCache * kSelThreads; i < nvirt; i += kSelThreads) {
-      const int slot = i < n8 ? i : s.cap + (i - n8);
-      const int p = pos[slot];
-      if (i >= n8 && p < 0) continue;
-      nring += (i >= n8);
-      float Ai = 0.f;
-      for (int h = 0; h < s.Hkv; ++h) Ai += __ldg(&d.mass[(lb * s.Hkv + h) * s.S + slot]);
-      const float a = fmaf(lam, ema[slot], (1.0f - lam) * (Ai * inv_hq));
-      ema[slot] = a;
-      if (p < thr) {
-        amin = fminf(amin, a); amax = fmaxf(amax, a);
-        pmin = min(pmin, p); pmax = max(pmax, p);
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int q = q0 + r * kSelThreads;
+      if (q >= nq) continue;
+      const bool ring = q >= q8;
+      const int slot0 = ring ? cap + 4 * (q - q8) : 4 * q;
+      const int pv[4] = {P4[r].x, P4[r].y, P4[r].z, P4[r].w};
+      const float ev[4] = {E4[r].x, E4[r].y, E4[r].z, E4[r].w};
+      const float av[4] = {A4[r].x, A4[r].y, A4[r].z, A4[r].w};
+      float nv[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int p = pv[j];
+        const bool valid = ring ? p >= 0 : 4 * q + j < n8;
+        nv[j] = ev[j];
+        int cp = INT_MAX;
+        if (valid) {
+          const float a = fmaf(lam, ev[j], (1.0f - lam) * (av[j] * inv_hq));
+          nv[j] = a;
+          nring += ring;
+          if (p < thr) {
+            cp = p;
+            ++ncand;
+            amin = fminf(amin, a); amax = fmaxf(amax, a);
+            pmin = min(pmin, p); pmax = max(pmax, p);
+          }
+        }
+        if (kSmemKeys) {
+          KEY[slot0 + j] = __float_as_uint(nv[j]);
+          SPOS[slot0 + j] = cp;
+        }
       }
+      *reinterpret_cast<float4*>(ema + slot0) = make_float4(nv[0], nv[1], nv[2], nv[3]);
     }
   }
-  // one combined block reduction of (nring, amin, amax, pmin, pmax)
+  // one combined block reduction of (nring, ncand, amin, amax, pmin, pmax)
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     nring += __shfl_xor_sync(0xffffffffu, nring, o);
+    ncand += __shfl_xor_sync(0xffffffffu, ncand, o);
     amin = fminf(amin, __shfl_xor_sync(0xffffffffu, amin, o));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
     pmin = min(pmin, __shfl_xor_sync(0xffffffffu, pmin, o));
     pmax = max(pmax, __shfl_xor_sync(0xffffffffu, pmax, o));
   }
   if (lane == 0) {
-    red5i[warp][0] = nring; red5i[warp][1] = pmin; red5i[warp][2] = pmax;
-    red5f[warp][0] = amin; red5f[warp][1] = amax;
+    red_i[warp][0] = nring; red_i[warp][1] = ncand; red_i[warp][2] = pmin; red_i[warp][3] = pmax;
+    red_f[warp][0] = amin; red_f[warp][1] = amax;
   }
   __syncthreads();
-  nring = red5i[0][0]; pmin = red5i[0][1]; pmax = red5i[0][2];
-  amin = red5f[0][0]; amax = red5f[0][1];
+  nring = red_i[0][0]; ncand = red_i[0][1]; pmin = red_i[0][2]; pmax = red_i[0][3];
+  amin = red_f[0][0]; amax = red_f[0][1];
   for (int w = 1; w < kSelWarps; ++w) {
-    nring += red5i[w][0];
-    pmin = min(pmin, red5i[w][1]); pmax = max(pmax, red5i[w][2]);
-    amin = fminf(amin, red5f[w][0]); amax = fmaxf(amax, red5f[w][1]);
+    nring += red_i[w][0]; ncand += red_i[w][1];
+    pmin = min(pmin, red_i[w][2]); pmax = max(pmax, red_i[w][3]);
+    amin = fminf(amin, red_f[w][0]); amax = fmaxf(amax, red_f[w][1]);
   }
-  const int n = n8 + nring - 1;          // resident entries, new token excluded
-  const int k = max(0, n - N);
+  const int n = n8 + nring - 1;            // resident entries, new token excluded
+  const int kwant = max(0, n - N);
+  const int k = min(kwant, ncand);         // a budget below the protected window is flagged below
 
   // ------------------------------------------------ 3. rank and select
-  if (k > 0) {
-    const float arng = amax - amin;
-    const float prng = (float)(pmax - pmin);
-    const float alpha = s.alpha;
-    auto score_key = [&](float a, int p) -> uint32_t {
-      const float ah = arng > 0.f ? (a - amin) / arng : 0.f;
-      const float rh = prng > 0.f ? (float)(p - pmin) / prng : 0.f;
-      return __float_as_uint(alpha * ah + (1.0f - alpha) * rh);   // s >= 0: bits are monotone
-    };
+  // s = alpha a_hat + (1 - alpha) r_hat >= 0, so its float bits order like s.
+  const float arng = amax - amin, prng = (float)(pmax - pmin);
+  const float ia = arng > 0.f ? 1.0f / arng : 0.f, ip = prng > 0.f ? 1.0f / prng : 0.f;
+  const float alpha = s.alpha, beta = 1.0f - s.alpha;
+  // candidate position of element e (INT_MAX if none) and its score bits
+  auto cand_of = [&](int slot, bool int8) -> int {
+    if (kSmemKeys) return SPOS[slot];
+    const int p = pos[slot];
+    return ((int8 || p >= 0) && p < thr) ? p : INT_MAX;
+  };
+  auto key_of = [&](int slot, int p) -> uint32_t {
+    const float a = kSmemKeys ? __uint_as_float(KEY[slot]) : ema[slot];
+    return __float_as_uint(alpha * ((a - amin) * ia) + beta * ((float)(p - pmin) * ip));
+  };
+  uint32_t kpre = 0u, kmask = 0u, ppre = 0u, pmask = 0u;
+  bool kall = true;
+  if (k == 1) {
+    // ---------------------------------------------- one eviction: argmin of (s, position)
     unsigned long long best = ~0ull;
     int bslot = -1;
-#pragma unroll
-    for (int c = 0; c < kCache; ++c) {
-      const int i = threadIdx.x + c * kSelThreads;
-      const int p = cpos[c];
-      if (i >= nvirt || p < 0 || p >= thr) continue;
-      const int slot = i < n8 ? i : s.cap + (i - n8);
-      const uint32_t key = score_key(cema[c], p);
-      if (k > 1) keys[slot] = key;
-      const unsigned long long comp = ((unsigned long long)key << 32) | (uint32_t)p;
+    for (int e = threadIdx.x; e < nvirt; e += kSelThreads) {
+      const int slot = slot_of(e);
+      const int p = cand_of(slot, e < n8);
+      if (p == INT_MAX) continue;
+      const unsigned long long comp = ((unsigned long long)key_of(slot, p) << 32) | (uint32_t)p;
       if (comp < best) { best = comp; bslot = slot; }
     }
-    for (int i = threadIdx.x + kCache * kSelThreads; i < nvirt; i += kSelThreads) {
-      const int slot = i < n8 ? i : s.cap + (i - n8);
-      const int p = pos[slot];
-      if (p < 0 || p >= thr) continue;
-      const uint32_t key = score_key(ema[slot], p);
-      if (k > 1) keys[slot] = key;
-      const unsigned long long comp = ((unsigned long long)key << 32) | (uint32_t)p;
-      if (comp < best) { best = comp; bslot = slot; }
+    unsigned long long m = best;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long v = __shfl_xor_sync(0xffffffffu, m, o);
+      m = v < m ? v : m;
     }
-    if (k == 1) {
-      // ---------------------------------------------- one eviction: argmin
-      const unsigned long long thr1 = block_reduce(best, MinOp(), red64);
-      if (best == thr1 && bslot >= 0) s_evslot = bslot;   // composites are unique
+    if (lane == 0) red64[warp] = m;
+    __syncthreads();
+    m = red64[0];
+    for (int w = 1; w < kSelWarps; ++w) m = red64[w] < m ? red64[w] : m;
+    if (best == m && bslot >= 0) {   // composites are unique
+      s_evslot = bslot;
+      s_evpos = (int)(uint32_t)(m & 0xffffffffu);
+    }
+  } else if (k > 1) {
+    // ---------------------------------------------- k > 1: keys, then radix select
+    for (int e = threadIdx.x; e < nvirt; e += kSelThreads) {
+      const int slot = slot_of(e);
+      const int p = cand_of(slot, e < n8);
+      KEY[slot] = p == INT_MAX ? kNoKey : key_of(slot, p);
+    }
+    int rem = k;
+    kall = false;
+    for (int shift = 24; shift >= 0 && !kall; shift -= 8) {
+      hist[threadIdx.x] = 0;
       __syncthreads();
-      if (threadIdx.x == 0) {
-        const int es = s_evslot;
-        list[0] = (int)(uint32_t)(thr1 & 0xffffffffu);
-        s_cnt = 1;
-        if (es < s.cap) {
-          s_k8 = 1;
-        } else {
-          pos[es] = -1;   // evicted ring entry: the slot becomes empty
-        }
+      for (int e = threadIdx.x; e < nvirt; e += kSelThreads) {
+        const uint32_t key = KEY[slot_of(e)];
+        if ((key & kmask) == kpre) atomicAdd(&hist[(key >> shift) & 255u], 1);
       }
-    } else {
-      // ---------------------------------------------- k > 1: 64-bit radix select
-      for (int w = threadIdx.x; w < s.cap / 32; w += kSelThreads) bitmap[w] = 0u;
       __syncthreads();
-      if (threadIdx.x == 0) {
-        s_prefix = 0ull;
-        s_mask = 0ull;
-        s_remaining = k;
-      }
-      for (int shift = 56; shift >= 0; shift -= 8) {
-        for (int i = threadIdx.x; i < 256; i += kSelThreads) hist[i] = 0;
+      if (warp == 0) hist_find(hist, rem, lane, &s_digit, &s_rem, &s_dcnt);
+      __syncthreads();
+      kpre |= (uint32_t)s_digit << shift;
+      kmask |= 255u << shift;
+      rem = s_rem;
+      kall = s_dcnt == rem;                  // the whole bucket goes: no finer digit needed
+    }
+    if (!kall) {
+      // keys tie exactly at the cut: the rem oldest of them go
+      bool pall = false;
+      for (int shift = 24; shift >= 0 && !pall; shift -= 8) {
+        hist[threadIdx.x] = 0;
         __syncthreads();
-        const unsigned long long prefix = s_prefix, mask = s_mask;
-        for (int i = threadIdx.x; i < nvirt; i += kSelThreads) {
-          const int slot = i < n8 ? i : s.cap + (i - n8);
-          const int p = pos[slot];
-          if (p < 0 || p >= thr) continue;
-          const unsigned long long comp = ((unsigned long long)keys[slot] << 32) | (uint32_t)p;
-          if ((comp & mask) == prefix) atomicAdd(&hist[(comp >> shift) & 255], 1);
+        for (int e = threadIdx.x; e < nvirt; e += kSelThreads) {
+          const int slot = slot_of(e);
+          if (KEY[slot] != kpre) continue;
+          const uint32_t p = (uint32_t)cand_of(slot, e < n8);
+          if ((p & pmask) == ppre) atomicAdd(&hist[(p >> shift) & 255u], 1);
         }
         __syncthreads();
-        if (warp == 0) {
-          // find the digit at which the running count reaches `remaining`
-          const int rem = s_remaining;
-          int cnt[8], run = 0;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            cnt[j] = hist[lane * 8 + j];
-            run += cnt[j];
-          }
-          int incl = run;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-          }
-          int before = incl - run;
-          if (before < rem && rem <= incl) {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              if (before < rem && rem <= before + cnt[j]) {
-                s_digit = lane * 8 + j;
-                s_remaining = rem - before;
-                // all elements with this digit are taken: stop refining
-                if (cnt[j] == rem - before) s_remaining = -(rem - before);
-              }
-              before += cnt[j];
-            }
-          }
-        }
+        if (warp == 0) hist_find(hist, rem, lane, &s_digit, &s_rem, &s_dcnt);
         __syncthreads();
-        if (threadIdx.x == 0) {
-          s_prefix |= (unsigned long long)s_digit << shift;
-          s_mask |= 255ull << shift;
-        }
-        __syncthreads();
-        if (s_remaining < 0) break;
-      }
-      const unsigned long long threshold = s_prefix | ~s_mask;
-      // -------------------------------------------- 4. mark the evicted
-      for (int i = threadIdx.x; i < nvirt; i += kSelThreads) {
-        const int slot = i < n8 ? i : s.cap + (i - n8);
-        const int p = pos[slot];
-        if (p < 0 || p >= thr) continue;
-        const unsigned long long comp = ((unsigned long long)keys[slot] << 32) | (uint32_t)p;
-        if (comp > threshold) continue;
-        const int idx = atomicAdd(&s_cnt, 1);
-        if (idx < sort_cap) list[idx] = p;
-        if (i < n8) {
-          atomicOr(&bitmap[slot >> 5], 1u << (slot & 31));
-          atomicAdd(&s_k8, 1);
-        } else {
-          pos[slot] = -1;   // evicted ring entry: the slot becomes empty
-        }
+        ppre |= (uint32_t)s_digit << shift;
+        pmask |= 255u << shift;
+        rem = s_rem;
+        pall = s_dcnt == rem;
       }
     }
+  }
+  // element selected by the radix select (k > 1)
+  auto evicted = [&](int slot, bool int8, int& p) -> bool {
+    const uint32_t key = KEY[slot];
+    if (key == kNoKey) return false;
+    const uint32_t mk = key & kmask;
+    if (mk > kpre) return false;
+    p = cand_of(slot, int8);
+    if (mk < kpre || kall) return true;
+    return ((uint32_t)p & pmask) <= ppre;
+  };
+
+  // ------------------------------------------------ 4. sorted evicted positions
+  int32_t* ev = evicted_out + lb * s.max_evict;
+  if (k == 1) {
+    __syncthreads();
+    if (threadIdx.x == 0 && s.max_evict > 0) ev[0] = s_evpos;
+  } else if (k > 1) {
+    int out_base = 0;
+    for (long long wb = pmin; wb < thr; wb += 32ll * kPosWords) {
+      const int base = (int)wb;
+      const int nwords = (int)min((long long)kPosWords, ((long long)thr - wb + 31) / 32);
+      for (int w = threadIdx.x; w < nwords; w += kSelThreads) posbits[w] = 0u;
+      __syncthreads();
+      for (int e = threadIdx.x; e < nvirt; e += kSelThreads) {
+        const int slot = slot_of(e);
+        int p = 0;
+        if (!evicted(slot, e < n8, p)) continue;
+        const long long off = (long long)p - base;
+        if (off >= 0 && off < 32ll * nwords) atomicOr(&posbits[off >> 5], 1u << (off & 31));
+      }
+      __syncthreads();
+      // each thread owns 8 consecutive words; block exclusive scan of their counts
+      constexpr int kWpt = kPosWords / kSelThreads;
+      const int w0 = threadIdx.x * kWpt;
+      int mine = 0;
+#pragma unroll
+      for (int j = 0; j < kWpt; ++j) mine += (w0 + j < nwords) ? __popc(posbits[w0 + j]) : 0;
+      int incl = mine;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (lane == 31) scan_w[warp] = incl;
+      __syncthreads();
+      int off = out_base + incl - mine, total = 0;
+      for (int w = 0; w < kSelWarps; ++w) {
+        if (w < warp) off += scan_w[w];
+        total += scan_w[w];
+      }
+#pragma unroll
+      for (int j = 0; j < kWpt; ++j) {
+        if (w0 + j >= nwords) break;
+        uint32_t bits = posbits[w0 + j];
+        while (bits) {
+          const int bit = __ffs(bits) - 1;
+          bits &= bits - 1;
+          if (off < s.max_evict) ev[off] = base + 32 * (w0 + j) + bit;
+          ++off;
+        }
+      }
+      out_base += total;
+      __syncthreads();
+    }
+    // apply: INT8 evictions into the bitmap, ring evictions empty their slot
+    int mycnt = 0, myk8 = 0;
+    for (int e = threadIdx.x; e < nvirt; e += kSelThreads) {
+      const int slot = slot_of(e);
+      int p = 0;
+      if (!evicted(slot, e < n8, p)) continue;
+      ++mycnt;
+      if (e < n8) {
+        atomicOr(&bm8[slot >> 5], 1u << (slot & 31));
+        ++myk8;
+      } else {
+        pos[slot] = -1;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      mycnt += __shfl_xor_sync(0xffffffffu, mycnt, o);
+      myk8 += __shfl_xor_sync(0xffffffffu, myk8, o);
+    }
+    if (lane == 0 && mycnt) atomicAdd(&s_cnt, mycnt);
+    if (lane == 0 && myk8) atomicAdd(&s_k8, myk8);
+  }
+  if (k == 1 && threadIdx.x == 0) {
+    s_cnt = 1;
+    s_k8 = s_evslot < cap ? 1 : 0;
   }
   __syncthreads();
   const int cnt = s_cnt;
-  if (threadIdx.x == 0 && cnt != k) atomicOr(d.status, kStatusBadCount);
-  if (threadIdx.x == 0 && cnt > s.max_evict) atomicOr(d.status, kStatusEvictBound);
+  const int k8 = s_k8;
+  if (threadIdx.x == 0) {
+    nevict_out[lb] = cnt;
+    if (cnt != kwant) atomicOr(d.status, kStatusBadCount);
+    if (cnt > s.max_evict) atomicOr(d.status, kStatusEvictBound);
+  }
 
-  // ------------------------------------------------ 5. sorted evicted positions
-  const int nlist = min(cnt, min(sort_cap, s.max_evict));
-  if (nlist > 1) {
-    int np2 = 1;
-    while (np2 < nlist) np2 <<= 1;
-    for (int i = nlist + threadIdx.x; i < np2; i += kSelThreads) list[i] = INT_MAX;
+  // ------------------------------------------------ 5. compaction and requantisation
+  const int n8p = n8 - k8;
+  int moves = 0;
+  const size_t u0 = unit_index(s, l, b, 0);
+  const size_t ustride8 = (size_t)s.cstride * D;        // INT8 bytes per unit
+  const size_t ustride16 = (size_t)WR * D * 2;          // FP16 ring bytes per unit
+  bool req;
+  if (k <= 1) {
+    req = tl >= 0 && prs == tl && s_evslot != rslot;
+  } else {
+    req = tl >= 0 && pos[rslot] == tl;   // a ring eviction of this step already cleared it
+  }
+  if (req && n8p >= cap && threadIdx.x == 0) atomicOr(d.status, kStatusCapacity);
+  const bool do_req = req && n8p < cap;
+  const int kw = lane >> 2, kt = lane & 3;   // K word of this lane: channels 16kw + 2kt + {0,1,8,9}
+  const int kc0 = 16 * kw + 2 * kt;
+  constexpr int kVPerLane = D / 32;
+
+  if (k > 1 && k8 > 0) {
+    // ---------------------------------------------- tail fill: holes < n8p <- survivors >= n8p
+    uint32_t* hole = KEY;                 // [moves]
+    uint32_t* mover = KEY + (S >> 1);     // [moves]
+    const int nw = (n8 + 31) >> 5;
+    int base_h = 0, base_m = 0;
+    for (int w0 = 0; w0 < nw; w0 += kSelThreads) {
+      const int w = w0 + threadIdx.x;
+      uint32_t hb = 0u, mb = 0u;
+      if (w < nw) {
+        const uint32_t bits = bm8[w];
+        // slots of this word below n8p (holes are evicted ones) and in [n8p, n8) (movers survive)
+        const int lo = w * 32;
+        const uint32_t below = n8p <= lo ? 0u : (n8p >= lo + 32 ? 0xffffffffu : ((1u << (n8p - lo)) - 1u));
+        const uint32_t inreg = n8 >= lo + 32 ? 0xffffffffu : ((1u << (n8 - lo)) - 1u);
+        hb = bits & below;
+        mb = ~bits & inreg & ~below;
+      }
+      const int ch = __popc(hb), cm = __popc(mb);
+      int ih = ch, im = cm;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int vh = __shfl_up_sync(0xffffffffu, ih, o);
+        const int vm = __shfl_up_sync(0xffffffffu, im, o);
+        if (lane >= o) { ih += vh; im += vm; }
+      }
+      __syncthreads();
+      if (lane == 31) { red_i[warp][0] = ih; red_i[warp][1] = im; }
+      __syncthreads();
+      int offh = base_h, offm = base_m, th = 0, tm = 0;
+      for (int ww = 0; ww < kSelWarps; ++ww) {
+        if (ww < warp) { offh += red_i[ww][0]; offm += red_i[ww][1]; }
+        th += red_i[ww][0];
+        tm += red_i[ww][1];
+      }
+      int rh = offh + ih - ch, rm = offm + im - cm;
+      while (hb) { const int j = __ffs(hb) - 1; hb &= hb - 1; hole[rh++] = w * 32 + j; }
+      while (mb) { const int j = __ffs(mb) - 1; mb &= mb - 1; mover[rm++] = w * 32 + j; }
+      base_h += th;
+      base_m += tm;
+    }
+    moves = base_h;
     __syncthreads();
-    for (int size = 2; size <= np2; size <<= 1) {
-      for (int stride = size >> 1; stride > 0; stride >>= 1) {
-        for (int i = threadIdx.x; i < np2; i += kSelThreads) {
-          const int j = i ^ stride;
-          if (j > i) {
-            const bool up = (i & size) == 0;
-            const int a = list[i], c = list[j];
-            if ((a > c) == up) {
-              list[i] = c;
-              list[j] = a;
-            }
-          }
+    // one warp per move, four KV heads at a time: every load before any store
+    for (int mv = warp; mv < moves; mv += kSelWarps) {
+      const int src = (int)mover[mv], dst = (int)hole[mv];
+      if (lane == 0) {
+        pos[dst] = pos[src];
+        ema[dst] = ema[src];
+      }
+      const size_t sblk = (size_t)(src >> 4) * 16 * D, dblk = (size_t)(dst >> 4) * 16 * D;
+      const int sk_off = k8_offset(D, src & 15, kc0), dk_off = k8_offset(D, dst & 15, kc0);
+      for (int h0 = 0; h0 < Hkv; h0 += 4) {
+        uint32_t kwv[4];
+        uint8_t vbv[4][kVPerLane];
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh) {
+          if (h0 + hh >= Hkv) break;
+          const uint8_t* k8u = d.k8 + (u0 + h0 + hh) * ustride8 + sblk;
+          const uint8_t* v8u = d.v8 + (u0 + h0 + hh) * ustride8 + sblk;
+          if (lane < D / 4) kwv[hh] = *reinterpret_cast<const uint32_t*>(k8u + sk_off);
+#pragma unroll
+          for (int i = 0; i < kVPerLane; ++i) vbv[hh][i] = v8u[v8_offset(D, src & 15, lane + 32 * i)];
         }
-        __syncthreads();
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh) {
+          if (h0 + hh >= Hkv) break;
+          uint8_t* k8u = d.k8 + (u0 + h0 + hh) * ustride8 + dblk;
+          uint8_t* v8u = d.v8 + (u0 + h0 + hh) * ustride8 + dblk;
+          if (lane < D / 4) *reinterpret_cast<uint32_t*>(k8u + dk_off) = kwv[hh];
+#pragma unroll
+          for (int i = 0; i < kVPerLane; ++i) v8u[v8_offset(D, dst & 15, lane + 32 * i)] = vbv[hh][i];
+        }
+      }
+    }
+    __syncthreads();   // a mover may sit in slot n8p, which the requantisation rewrites
+  }
+
+  // one eviction from the INT8 region: move slot n8 - 1 into the hole (same
+  // lanes as the requantisation below, which may rewrite slot n8 - 1)
+  const int dst1 = s_evslot, src1 = n8 - 1;
+  const bool move1 = k == 1 && k8 == 1 && dst1 < src1;
+  if (move1) moves = 1;
+  const char* k16b = reinterpret_cast<const char*>(d.k16);
+  const char* v16b = reinterpret_cast<const char*>(d.v16);
+  if (move1 || do_req) {
+    const size_t sblk = (size_t)(src1 >> 4) * 16 * D, dblk = (size_t)(dst1 >> 4) * 16 * D;
+    const size_t qblk = (size_t)(n8p >> 4) * 16 * D;
+    const size_t rblk = (size_t)(rs >> 4) * 16 * D * 2;
+    for (int h = warp; h < Hkv; h += kSelWarps) {
+      const size_t u = u0 + h;
+      uint8_t* k8u = d.k8 + u * ustride8;
+      uint8_t* v8u = d.v8 + u * ustride8;
+      if (move1) {
+        uint32_t kv = 0u;
+        uint8_t vb[kVPerLane];
+        if (lane < D / 4) kv = *reinterpret_cast<const uint32_t*>(k8u + sblk + k8_offset(D, src1 & 15, kc0));
+#pragma unroll
+        for (int i = 0; i < kVPerLane; ++i) vb[i] = v8u[sblk + v8_offset(D, src1 & 15, lane + 32 * i)];
+        if (lane < D / 4) *reinterpret_cast<uint32_t*>(k8u + dblk + k8_offset(D, dst1 & 15, kc0)) = kv;
+#pragma unroll
+        for (int i = 0; i < kVPerLane; ++i) v8u[dblk + v8_offset(D, dst1 & 15, lane + 32 * i)] = vb[i];
+      }
+      if (do_req) {
+        const char* rk = k16b + u * ustride16 + rblk;
+        const char* rv = v16b + u * ustride16 + rblk;
+        const float* sKu = d.sK + u * D;
+        const float* sVu = d.sV + u * D;
+        uint2 xk = make_uint2(0u, 0u);
+        float2 s01 = make_float2(1.f, 1.f), s89 = make_float2(1.f, 1.f);
+        unsigned short xv[kVPerLane];
+        float sv[kVPerLane];
+        if (lane < D / 4) {
+          xk = *reinterpret_cast<const uint2*>(rk + k16_offset(D, rs & 15, kc0));
+          s01 = *reinterpret_cast<const float2*>(sKu + kc0);
+          s89 = *reinterpret_cast<const float2*>(sKu + kc0 + 8);
+        }
+#pragma unroll
+        for (int i = 0; i < kVPerLane; ++i) {
+          xv[i] = *reinterpret_cast<const unsigned short*>(rv + v16_offset(D, rs & 15, lane + 32 * i));
+          sv[i] = sVu[lane + 32 * i];
+        }
+        if (lane < D / 4) {
+          const uint32_t w =
+              quant_code_sel(__half2float(__ushort_as_half((unsigned short)(xk.x & 0xffffu))), s01.x) |
+              quant_code_sel(__half2float(__ushort_as_half((unsigned short)(xk.x >> 16))), s01.y) << 8 |
+              quant_code_sel(__half2float(__ushort_as_half((unsigned short)(xk.y & 0xffffu))), s89.x) << 16 |
+              quant_code_sel(__half2float(__ushort_as_half((unsigned short)(xk.y >> 16))), s89.y) << 24;
+          *reinterpret_cast<uint32_t*>(k8u + qblk + k8_offset(D, n8p & 15, kc0)) = w;
+        }
+#pragma unroll
+        for (int i = 0; i < kVPerLane; ++i)
+          v8u[qblk + v8_offset(D, n8p & 15, lane + 32 * i)] =
+              (uint8_t)quant_code_sel(__half2float(__ushort_as_half(xv[i])), sv[i]);
       }
     }
   }
-  int32_t* ev = evicted_out + lb * s.max_evict;
-  for (int i = threadIdx.x; i < nlist; i += kSelThreads) ev[i] = list[i];
-  if (threadIdx.x == 0) nevict_out[lb] = cnt;
-
-  // ------------------------------------------------ 6. compaction (tail fill)
-  const int k8 = s_k8;
-  const int n8p = n8 - k8;
-  int moves = 0;
-  const int D = s.D;
-  const int tl = t - s.W;                      // position leaving the FP16 window
-  const int rs = tl >= 0 ? tl % s.WR : 0;
-  const int rslot = s.cap + rs;
-  // pos[rslot] is final here: a ring eviction of this step already cleared it
-  const bool req = tl >= 0 && pos[rslot] == tl;
-  if (req && n8p >= s.cap && threadIdx.x == 0) atomicOr(d.status, kStatusCapacity);
-  const bool do_req = req && n8p < s.cap;
-  if (k <= 1) {
-    // ---------------------------------------------- 6+7. at most one move, then requant
-    // The move reads slot n8 - 1 and the requant writes slot n8p, which can be
-    // the same slot: every thread loads first, the block synchronises, then
-    // every thread stores.
-    const int dst = s_evslot, src = n8 - 1;
-    const bool do_move = k == 1 && k8 == 1 && dst < src;
-    moves = do_move ? 1 : 0;
-    const int per_tok = D / 4 + D;             // K words + V bytes per head
-    constexpr int kMv = 8;                     // move items per thread (Hkv*per_tok <= 8*256)
-    constexpr int kRq = 8;                     // requant channels per thread (Hkv*D <= 8*256)
-    if (s.Hkv * per_tok > kMv * kSelThreads || s.Hkv * D > kRq * kSelThreads) {
-      // many KV heads: move first, then requantise (slot n8 - 1 is read before it is rewritten)
-      for (int i = threadIdx.x; do_move && i < s.Hkv * per_tok; i += kSelThreads) {
-        const int h = i / per_tok, e = i % per_tok;
-        const size_t u = unit_index(s, l, b, h);
-        uint8_t* k8u = d.k8 + u * (size_t)s.cstride * D;
-        uint8_t* v8u = d.v8 + u * (size_t)s.cstride * D;
-        if (e < D / 4) {
-          const int c0 = (e / 4) * 16 + 2 * (e % 4);
-          *reinterpret_cast<uint32_t*>(k8u + (size_t)(dst >> 4) * 16 * D + k8_offset(D, dst & 15, c0)) =
-              *reinterpret_cast<const uint32_t*>(k8u + (size_t)(src >> 4) * 16 * D + k8_offset(D, src & 15, c0));
-        } else {
-          const int c = e - D / 4;
-          v8u[(size_t)(dst >> 4) * 16 * D + v8_offset(D, dst & 15, c)] =
-              v8u[(size_t)(src >> 4) * 16 * D + v8_offset(D, src & 15, c)];
-        }
-      }
-      int mpos = 0;
-      float mema = 0.f;
-      if (threadIdx.x == 0 && do_move) { mpos = pos[src]; mema = ema[src]; }
-      __syncthreads();
-      if (threadIdx.x == 0 && do_move) { pos[dst] = mpos; ema[dst] = mema; }
-      const char* k16b = reinterpret_cast<const char*>(d.k16);
-      const char* v16b = reinterpret_cast<const char*>(d.v16);
-      for (int i = threadIdx.x; do_req && i < s.Hkv * D; i += kSelThreads) {
-        const int h = i / D, c = i % D;
-        const size_t u = unit_index(s, l, b, h);
-        const size_t rblk = (u * (s.WR / 16) + (rs >> 4)) * 16 * D * 2;
-        const float xk = __half2float(*reinterpret_cast<const __half*>(k16b + rblk + k16_offset(D, rs & 15, c)));
-        const float xv = __half2float(*reinterpret_cast<const __half*>(v16b + rblk + v16_offset(D, rs & 15, c)));
-        const size_t dblk = (u * (size_t)(s.cstride / 16) + (n8p >> 4)) * 16 * D;
-        d.k8[dblk + k8_offset(D, n8p & 15, c)] = quant_code_sel(xk, d.sK[u * D + c]);
-        d.v8[dblk + v8_offset(D, n8p & 15, c)] = quant_code_sel(xv, d.sV[u * D + c]);
-      }
-      float rema = 0.f;
-      if (threadIdx.x == 0 && do_req) rema = ema[rslot];
-      __syncthreads();
-      if (threadIdx.x == 0 && do_req) { pos[n8p] = tl; ema[n8p] = rema; pos[rslot] = -1; }
-    } else {
-    // every load of this phase is issued before any value is used
-    uint32_t mv[kMv];
-    unsigned short xk[kRq], xv[kRq];
-    float sk[kRq], sv[kRq];
-#pragma unroll
-    for (int j = 0; j < kMv; ++j) {
-      const int i = threadIdx.x + j * kSelThreads;
-      mv[j] = 0u;
-      if (do_move && i < s.Hkv * per_tok) {
-        const int h = i / per_tok, e = i % per_tok;
-        const size_t u = unit_index(s, l, b, h);
-        const uint8_t* k8u = d.k8 + u * (size_t)s.cstride * D;
-        const uint8_t* v8u = d.v8 + u * (size_t)s.cstride * D;
-        if (e < D / 4)
-          mv[j] = *reinterpret_cast<const uint32_t*>(k8u + (size_t)(src >> 4) * 16 * D +
-                                                     k8_offset(D, src & 15, (e / 4) * 16 + 2 * (e % 4)));
-        else
-          mv[j] = v8u[(size_t)(src >> 4) * 16 * D + v8_offset(D, src & 15, e - D / 4)];
-      }
-    }
-    const char* k16b = reinterpret_cast<const char*>(d.k16);
-    const char* v16b = reinterpret_cast<const char*>(d.v16);
-#pragma unroll
-    for (int j = 0; j < kRq; ++j) {
-      const int i = threadIdx.x + j * kSelThreads;
-      xk[j] = xv[j] = 0;
-      sk[j] = sv[j] = 1.f;
-      if (do_req && i < s.Hkv * D) {
-        const int h = i / D, c = i % D;
-        const size_t u = unit_index(s, l, b, h);
-        const size_t rblk = (u * (s.WR / 16) + (rs >> 4)) * 16 * D * 2;
-        xk[j] = *reinterpret_cast<const unsigned short*>(k16b + rblk + k16_offset(D, rs & 15, c));
-        xv[j] = *reinterpret_cast<const unsigned short*>(v16b + rblk + v16_offset(D, rs & 15, c));
-        sk[j] = d.sK[u * D + c];
-        sv[j] = d.sV[u * D + c];
-      }
-    }
-    int mpos = 0;
-    float mema = 0.f, rema = 0.f;
-    if (threadIdx.x == 0) {
-      if (do_move) { mpos = pos[src]; mema = ema[src]; }
-      if (do_req) rema = ema[rslot];
-    }
-    __syncthreads();
-#pragma unroll
-    for (int j = 0; j < kMv; ++j) {
-      const int i = threadIdx.x + j * kSelThreads;
-      if (do_move && i < s.Hkv * per_tok) {
-        const int h = i / per_tok, e = i % per_tok;
-        const size_t u = unit_index(s, l, b, h);
-        uint8_t* k8u = d.k8 + u * (size_t)s.cstride * D;
-        uint8_t* v8u = d.v8 + u * (size_t)s.cstride * D;
-        if (e < D / 4)
-          *reinterpret_cast<uint32_t*>(k8u + (size_t)(dst >> 4) * 16 * D +
-                                       k8_offset(D, dst & 15, (e / 4) * 16 + 2 * (e % 4))) = mv[j];
-        else
-          v8u[(size_t)(dst >> 4) * 16 * D + v8_offset(D, dst & 15, e - D / 4)] = (uint8_t)mv[j];
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kRq; ++j) {
-      const int i = threadIdx.x + j * kSelThreads;
-      if (do_req && i < s.Hkv * D) {
-        const int h = i / D, c = i % D;
-        const size_t u = unit_index(s, l, b, h);
-        const size_t dblk = (u * (size_t)(s.cstride / 16) + (n8p >> 4)) * 16 * D;
-        d.k8[dblk + k8_offset(D, n8p & 15, c)] = quant_code_sel(__half2float(__ushort_as_half(xk[j])), sk[j]);
-        d.v8[dblk + v8_offset(D, n8p & 15, c)] = quant_code_sel(__half2float(__ushort_as_half(xv[j])), sv[j]);
-      }
-    }
-    if (threadIdx.x == 0) {
-      if (do_move) { pos[dst] = mpos; ema[dst] = mema; }
-      if (do_req) { pos[n8p] = tl; ema[n8p] = rema; pos[rslot] = -1; }
-    }
-    }
-  } else {
-    // ---------------------------------------------- 6. compaction (tail fill), k > 1
-    if (k8 > 0) {
-      // holes: evicted slots < n8p; movers: surviving slots in [n8p, n8).
-      uint32_t* hole = keys;                       // [moves]
-      uint32_t* mover = keys + (s.S >> 1);         // [moves]
-      const int nw = (n8 + 31) >> 5;
-      int base_h = 0, base_m = 0;
-      for (int w0 = 0; w0 < nw; w0 += kSelThreads) {
-        const int w = w0 + threadIdx.x;
-        uint32_t hb = 0u, mb = 0u;
-        if (w < nw) {
-          const uint32_t bits = bitmap[w];
-          for (int j = 0; j < 32; ++j) {
-            const int slot = w * 32 + j;
-            if (slot < n8p) hb |= ((bits >> j) & 1u) << j;
-            else if (slot < n8) mb |= ((~bits >> j) & 1u) << j;
-          }
-        }
-        // exclusive scans of the per-word counts across the block
-        int ch = __popc(hb), cm = __popc(mb);
-        int ih = ch, im = cm;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const int vh = __shfl_up_sync(0xffffffffu, ih, o);
-          const int vm = __shfl_up_sync(0xffffffffu, im, o);
-          if (lane >= o) { ih += vh; im += vm; }
-        }
-        __syncthreads();
-        if (lane == 31) { redi[warp] = ih; red64[warp] = (unsigned long long)im; }
-        __syncthreads();
-        int offh = base_h, offm = base_m;
-        for (int ww = 0; ww < warp; ++ww) { offh += redi[ww]; offm += (int)red64[ww]; }
-        int rh = offh + ih - ch, rm = offm + im - cm;
-        while (hb) { const int j = __ffs(hb) - 1; hb &= hb - 1; hole[rh++] = w * 32 + j; }
-        while (mb) { const int j = __ffs(mb) - 1; mb &= mb - 1; mover[rm++] = w * 32 + j; }
-        int th = 0, tm = 0;
-        for (int ww = 0; ww < kSelWarps; ++ww) { th += redi[ww]; tm += (int)red64[ww]; }
-        __syncthreads();
-        base_h += th;
-        base_m += tm;
-      }
-      moves = base_h;
-      __syncthreads();
-      const int per_tok = D / 4 + D;             // K words + V bytes per head
-      const long long total = (long long)moves * s.Hkv * per_tok;
-      for (long long i = threadIdx.x; i < total; i += kSelThreads) {
-        const int r = (int)(i / (s.Hkv * per_tok));
-        const int rest = (int)(i % (s.Hkv * per_tok));
-        const int h = rest / per_tok, e = rest % per_tok;
-        const int src = (int)mover[r], dst = (int)hole[r];
-        const size_t u = unit_index(s, l, b, h);
-        uint8_t* k8u = d.k8 + u * (size_t)s.cstride * D;
-        uint8_t* v8u = d.v8 + u * (size_t)s.cstride * D;
-        if (e < D / 4) {
-          // one 32-bit word = channels {16kk+2t, +1, +8, +9} of the token
-          const int c0 = (e / 4) * 16 + 2 * (e % 4);
-          const uint32_t wv = *reinterpret_cast<const uint32_t*>(
-              k8u + (size_t)(src >> 4) * 16 * D + k8_offset(D, src & 15, c0));
-          *reinterpret_cast<uint32_t*>(k8u + (size_t)(dst >> 4) * 16 * D + k8_offset(D, dst & 15, c0)) = wv;
-        } else {
-          const int c = e - D / 4;
-          v8u[(size_t)(dst >> 4) * 16 * D + v8_offset(D, dst & 15, c)] =
-              v8u[(size_t)(src >> 4) * 16 * D + v8_offset(D, src & 15, c)];
-        }
-        if (h == 0 && e == 0) {
-          pos[dst] = pos[src];
-          ema[dst] = ema[src];
-        }
-      }
-    }
-    __syncthreads();
-    // ---------------------------------------------- 7. requantise the entry leaving the window
-    if (do_req) {
-      const char* k16b = reinterpret_cast<const char*>(d.k16);
-      const char* v16b = reinterpret_cast<const char*>(d.v16);
-      for (int i = threadIdx.x; i < s.Hkv * D; i += kSelThreads) {
-        const int h = i / D, c = i % D;
-        const size_t u = unit_index(s, l, b, h);
-        const size_t rblk = (u * (s.WR / 16) + (rs >> 4)) * 16 * D * 2;
-        const float xk = __half2float(*reinterpret_cast<const __half*>(k16b + rblk + k16_offset(D, rs & 15, c)));
-        const float xv = __half2float(*reinterpret_cast<const __half*>(v16b + rblk + v16_offset(D, rs & 15, c)));
-        const size_t dblk = (u * (size_t)(s.cstride / 16) + (n8p >> 4)) * 16 * D;
-        d.k8[dblk + k8_offset(D, n8p & 15, c)] = quant_code_sel(xk, d.sK[u * D + c]);
-        d.v8[dblk + v8_offset(D, n8p & 15, c)] = quant_code_sel(xv, d.sV[u * D + c]);
-      }
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        pos[n8p] = tl;
-        ema[n8p] = ema[rslot];
-        pos[rslot] = -1;
-      }
-    }
+  if (threadIdx.x == 0) {
+    // metadata: every read before any write (slot n8 - 1 can be both)
+    const int mpos = move1 ? pos[src1] : 0;
+    const float mema = move1 ? ema[src1] : 0.f;
+    const float rema = do_req ? ema[rslot] : 0.f;
+    if (k == 1 && dst1 >= cap) pos[dst1] = -1;   // evicted ring entry: the slot becomes empty
+    if (move1) { pos[dst1] = mpos; ema[dst1] = mema; }
+    if (do_req) { pos[n8p] = tl; ema[n8p] = rema; pos[rslot] = -1; }
   }
   const int n8n = n8p + (do_req ? 1 : 0);
   const int requant = do_req ? 1 : 0;
   if (threadIdx.x == 0) {
     d.n8[lb] = n8n;
     // algorithmic bytes of this (layer, sequence)
-    const unsigned long long D = s.D, Hkv = s.Hkv, Hq = s.Hq;
+    const unsigned long long Dl = D, Hk = Hkv, Hq = s.Hq;
     const unsigned long long nres = (unsigned long long)n8 + nring;   // incl. new token
-    const unsigned long long attn = Hkv * D * (2ull * n8 + 4ull * nring) + 2ull * Hkv * D * 4 +
-                                    Hq * D * (2 + 4) + Hkv * nres * 4;
-    unsigned long long step_b = attn + nres * (4 + 4 + 4 + 4 * Hkv) + 2ull * Hkv * D * 2 * 2 +
-                                (unsigned long long)requant * 2 * Hkv * D * 3 +
-                                (unsigned long long)moves * (2 * Hkv * D + 8) * 2 +
+    const unsigned long long attn = Hk * Dl * (2ull * n8 + 4ull * nring) + 2ull * Hk * Dl * 4 +
+                                    Hq * Dl * (2 + 4) + Hk * nres * 4;
+    unsigned long long step_b = attn + nres * (4 + 4 + 4 + 4 * Hk) + 2ull * Hk * Dl * 2 * 2 +
+                                (unsigned long long)requant * 2 * Hk * Dl * 3 +
+                                (unsigned long long)moves * (2 * Hk * Dl + 8) * 2 +
                                 4ull * (cnt + 1);
     if (l == 0) step_b += (unsigned long long)s.V * 4;
     atomicAdd(&d.stats->evicted, (unsigned long long)cnt);
@@ -587,25 +607,50 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(Shape s, Dev d, 
   }
 }
 
-int launch_select(const Shape& s, const Dev& d, long long step, int32_t* evicted_pos,
-                  int32_t* n_evicted, int k_bound, cudaStream_t stream) {
-  int sort_cap = 1;
-  while (sort_cap < k_bound) sort_cap <<= 1;
-  if (sort_cap > s.max_evict) {
-    sort_cap = 1;
-    while (sort_cap < s.max_evict) sort_cap <<= 1;
+static SelSmem plan_select(const Shape& s) {
+  SelSmem p{};
+  size_t off = 0;
+  p.off_posbits = (int)off;
+  off += (size_t)kPosWords * 4;
+  p.off_bm8 = (int)off;
+  off += ((size_t)(s.cap / 32) * 4 + 15) & ~(size_t)15;
+  const size_t keys = (size_t)s.S * 4;
+  if (off + 2 * keys <= kSelSmemKeysMax) {
+    p.off_key = (int)off;
+    off += keys;
+    p.off_pos = (int)off;
+    off += keys;
+  } else {
+    p.off_key = p.off_pos = -1;
   }
-  const size_t smem = (size_t)(s.cap / 32) * 4 + (size_t)sort_cap * 4;
-  static size_t configured = 0;
-  if (smem > 48 * 1024 && smem > configured) {
-    if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
+  p.bytes = (int)off;
+  return p;
+}
+
+template <int D, bool kSmemKeys>
+static int launch_select_t(const Shape& s, const Dev& d, long long step, int32_t* evicted_pos,
+                           int32_t* n_evicted, const SelSmem& p, cudaStream_t stream) {
+  static int configured = 48 * 1024;
+  if (p.bytes > configured) {
+    if (cudaFuncSetAttribute(select_kernel<D, kSmemKeys>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             p.bytes) != cudaSuccess)
       return -1;
-    configured = smem;
+    configured = p.bytes;
   }
-  select_kernel<<<s.L * s.B, kSelThreads, smem, stream>>>(s, d, step, evicted_pos, n_evicted,
-                                                          sort_cap);
+  select_kernel<D, kSmemKeys><<<s.L * s.B, kSelThreads, p.bytes, stream>>>(s, d, step, evicted_pos,
+                                                                          n_evicted, p);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_select(const Shape& s, const Dev& d, long long step, int32_t* evicted_pos,
+                  int32_t* n_evicted, cudaStream_t stream) {
+  const SelSmem p = plan_select(s);
+  const bool smem_keys = p.off_key >= 0;
+  if (s.D == 128)
+    return smem_keys ? launch_select_t<128, true>(s, d, step, evicted_pos, n_evicted, p, stream)
+                     : launch_select_t<128, false>(s, d, step, evicted_pos, n_evicted, p, stream);
+  return smem_keys ? launch_select_t<64, true>(s, d, step, evicted_pos, n_evicted, p, stream)
+                   : launch_select_t<64, false>(s, d, step, evicted_pos, n_evicted, p, stream);
 }
 
 }  // namespace confkv

@@ -44,6 +44,7 @@ bool valid_config(const confkv_config* c) {
   if (!c || !c->n_high || !c->n_low) return false;
   if (c->L < 1 || c->B < 1 || c->Hq < 1 || c->Hkv < 1 || c->V < 2 || c->W < 1 || c->P < 0)
     return false;
+  if ((long long)c->V > 4096LL * kMaxSV) return false;   // vocabulary chunks of <= 4096 logits
   if (c->Hq % c->Hkv != 0 || c->Hq / c->Hkv > kMaxG) return false;
   if (c->d != 64 && c->d != 128) return false;
   if (c->cap < 16 || c->max_evict < 0) return false;
@@ -72,13 +73,9 @@ Shape make_shape(const confkv_config* c) {
   s.P = c->P;
   s.S = s.cap + s.WR;
   s.cstride = s.cap + 16;
-  // vocabulary chunks per sequence: <= 4096 logits each, and enough blocks
-  // in total to cover the GPU a few times over
-  const int min_sv = (c->V + 4095) / 4096;
-  const int want = (4 * kNumSMs + c->B - 1) / c->B;
-  int sv = std::min((c->V + 1023) / 1024, want);
-  sv = std::max(sv, min_sv);
-  s.SV = std::min(std::max(sv, 1), kMaxSV);
+  // vocabulary chunks per sequence: 4096 logits each (16 per thread of a
+  // 256-thread block); wider vocabularies than kMaxSV chunks are rejected
+  s.SV = std::min(std::max((c->V + 4095) / 4096, 1), kMaxSV);
   s.qbf16 = c->q_dtype == CONFKV_Q_BF16;
   s.max_evict = c->max_evict > 0 ? c->max_evict : s.cap + s.WR;
   s.tau = c->tau; s.wH = c->w_H; s.wm = c->w_m; s.wp = c->w_p;

@@ -84,8 +84,8 @@ struct ConfPartial {     // one vocab chunk of one sequence
   float M;               // chunk maximum
   float z1, z2;          // largest and second largest logit of the chunk
   int i1;                // index of z1 (lowest index on ties)
-  double S;              // sum exp(z - M)
-  double T;              // sum (z - M) exp(z - M)
+  float S, Se;           // sum exp(z - M) as an unevaluated sum S + Se
+  float T, Te;           // sum (z - M) exp(z - M) as T + Te
 };
 
 struct DevStats {        // cumulative counters, updated with atomics

@@ -84,7 +84,8 @@ typedef struct confkv_ctx confkv_ctx;
 
 /* Bytes of device workspace the context needs (state + scratch).  Returns
  * CONFKV_EINVAL for an invalid configuration: d not 64/128, Hq % Hkv != 0,
- * Hq / Hkv > 8, V < 2, some budget < P or < 1, cap < 16, W < 1. */
+ * Hq / Hkv > 8, V < 2 or V > 4096 * 1024, some budget < P or < 1, cap < 16,
+ * W < 1. */
 int confkv_workspace_bytes(const confkv_config* cfg, size_t* bytes);
 
 /* Create a context over `workspace` (device memory, >= the size above, 256-byte

@@ -87,7 +87,7 @@ def _cfg(**kw):
 
 
 @pytest.mark.parametrize("bad", [
-    dict(d=96), dict(Hq=6, Hkv=4), dict(Hq=18, Hkv=2), dict(V=1), dict(W=0),
+    dict(d=96), dict(Hq=6, Hkv=4), dict(Hq=18, Hkv=2), dict(V=1), dict(V=4096 * 1024 + 1), dict(W=0),
     dict(n_high=[4, 40]), dict(n_low=[80, 0]), dict(cap=8), dict(L=0), dict(B=0),
     dict(alpha=1.5), dict(lam=-0.1), dict(q_dtype=7), dict(P=-1),
 ])

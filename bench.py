@@ -28,6 +28,18 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "CONF-KV decode steps/s (all layers) + achieved HBM GB/s vs GB300 peak, 1 GPU"
+PROFILE_EVERY = 7   # at least this many timed steps per step that records per-kernel CUDA events
+
+
+def profile_stride(pool: int) -> int:
+    """Sampling stride for the per-kernel events: the smallest k >= PROFILE_EVERY
+    coprime with the input pool size, so that the sampled steps visit every
+    pool entry instead of a fixed subset of them."""
+    import math
+    k = PROFILE_EVERY
+    while math.gcd(k, max(pool, 1)) != 1:
+        k += 1
+    return k
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -257,7 +269,11 @@ def run_ours(args):
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
-    cache.profile_enable(args.steps)
+    # per-kernel events on every `every`-th timed step: an event record
+    # between kernels costs the stream ~2 us, so recording all four on every
+    # step would slow the very steps it times
+    every = profile_stride(R)
+    cache.profile_enable((args.steps + every - 1) // every, every)
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -350,6 +366,8 @@ def run_ours(args):
             "chain": chain,
             "breakdown_ms_per_step": {k: prof[k + "_ms"] / max(prof["steps"], 1)
                                       for k in ("prestep", "attention", "select")},
+            "kernel_timing": "CUDA events around each kernel on every %dth timed step (%d steps sampled)"
+                             % (every, prof["steps"]),
             "attention_launch": {"ctas_per_unit": splits, "smem_bytes": smem},
             "gpu_launches": 3 * args.steps,
             "clocks": clk,

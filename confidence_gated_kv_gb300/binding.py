@@ -82,7 +82,7 @@ def lib() -> ctypes.CDLL:
             "confkv_get_clock": (ctypes.c_int, [vp, vp, ctypes.POINTER(i64)]),
             "confkv_set_clock": (ctypes.c_int, [vp, vp, i64, vp]),
             "confkv_get_stats": (ctypes.c_int, [vp, ctypes.POINTER(Stats), vp]),
-            "confkv_profile_enable": (ctypes.c_int, [vp, i32]),
+            "confkv_profile_enable": (ctypes.c_int, [vp, i32, i32]),
             "confkv_profile_disable": (ctypes.c_int, [vp]),
             "confkv_profile_read": (ctypes.c_int, [vp] + [ctypes.POINTER(ctypes.c_double)] * 3 +
                                     [ctypes.POINTER(i32)]),
@@ -298,8 +298,10 @@ class Cache:
             _check(r, "confkv_get_stats")
         return {f: getattr(s, f) for f, _ in Stats._fields_}
 
-    def profile_enable(self, max_steps: int):
-        _check(lib().confkv_profile_enable(self._h, int(max_steps)), "confkv_profile_enable")
+    def profile_enable(self, max_steps: int, every: int = 1):
+        """Record per-kernel CUDA events on every `every`-th step (at most
+        `max_steps` recorded steps)."""
+        _check(lib().confkv_profile_enable(self._h, int(max_steps), int(every)), "confkv_profile_enable")
 
     def profile_disable(self):
         _check(lib().confkv_profile_disable(self._h), "confkv_profile_disable")

@@ -145,6 +145,8 @@ struct confkv_ctx {
   // profiling
   bool prof_on = false;
   int prof_max = 0, prof_count = 0;
+  int prof_every = 1;        // record every prof_every-th step
+  long long prof_tick = 0;   // steps seen while profiling is on
   std::vector<cudaEvent_t> ev;
 };
 
@@ -280,7 +282,8 @@ int confkv_step(confkv_ctx* ctx, const void* q, const void* k_new, const void* v
     if ((long long)ctx->T0[b] + ctx->steps >= (1LL << 31) - 1) return CONFKV_ECAPACITY;
 
   cudaStream_t st = as_stream(stream);
-  const bool prof = ctx->prof_on && ctx->prof_count < ctx->prof_max;
+  const bool prof = ctx->prof_on && ctx->prof_count < ctx->prof_max &&
+                    (ctx->prof_tick++ % ctx->prof_every) == 0;
   cudaEvent_t* ev = prof ? &ctx->ev[4 * ctx->prof_count] : nullptr;
   if (prof) cudaEventRecord(ev[0], st);
   if (launch_prestep(s, ctx->d, ctx->steps, logits, k_new, v_new, st) != 0) return CONFKV_ECUDA;
@@ -526,8 +529,10 @@ int confkv_get_stats(confkv_ctx* ctx, confkv_stats* out, void* stream) {
   return status ? CONFKV_EDEVICE : CONFKV_OK;
 }
 
-int confkv_profile_enable(confkv_ctx* ctx, int32_t max_steps) {
-  if (!ctx || max_steps < 1) return CONFKV_EINVAL;
+int confkv_profile_enable(confkv_ctx* ctx, int32_t max_steps, int32_t every) {
+  if (!ctx || max_steps < 1 || every < 1) return CONFKV_EINVAL;
+  ctx->prof_every = every;
+  ctx->prof_tick = 0;
   for (cudaEvent_t e : ctx->ev) cudaEventDestroy(e);
   ctx->ev.assign(4 * (size_t)max_steps, nullptr);
   for (auto& e : ctx->ev)

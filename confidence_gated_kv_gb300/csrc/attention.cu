@@ -752,6 +752,7 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
 
+  pdl_wait();
   if (threadIdx.x == 0) {
     s_abort = 0;
     for (int i = 0; i < stages; ++i) {
@@ -1091,9 +1092,10 @@ static int launch_d(const Shape& s, const Dev& d, const void* q, float* out, int
     }
     int grid = units < 2 * num_sms() ? units : 2 * num_sms();
     if (grid > d.score_ctas) grid = d.score_ctas;
-    attention_persistent_kernel<D><<<grid, kPThreads, smem, stream>>>(
-        s, d, q, out, budget, conf_out, stages_persistent(s));
-    return cudaGetLastError() == cudaSuccess ? 0 : -1;
+    return launch_pdl(attention_persistent_kernel<D>, dim3(grid), dim3(kPThreads), (size_t)smem, stream,
+                      s, d, q, out, budget, conf_out, stages_persistent(s)) == cudaSuccess
+               ? 0
+               : -1;
   }
   static bool configured_split = false;
   if (!configured_split) {

@@ -22,6 +22,7 @@
 #pragma once
 #include <cstdint>
 #include <cuda_fp16.h>
+#include <cuda_runtime.h>
 
 namespace confkv {
 
@@ -143,6 +144,37 @@ __host__ __device__ inline size_t unit_index(const Shape& s, int l, int b, int h
 __host__ __device__ inline size_t lb_index(const Shape& s, int l, int b) {
   return (size_t)l * s.B + b;
 }
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  The three kernels of a step (and the first
+// kernel of the next step) are launched with programmatic stream
+// serialisation, and each waits (griddepcontrol.wait) before its first global
+// memory access until the previous kernel has completed and its writes are
+// visible.  No kernel triggers its dependents early: the next grid is
+// launched as the CTAs of the current one exit, which saves part of the
+// launch gap (triggering at kernel entry instead measured about 5% slower per
+// step).  The data order is exactly the stream order; without the launch
+// attribute the wait does nothing.
+// ---------------------------------------------------------------------------
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+#endif
 
 // ---------------------------------------------------------------------------
 // Kernel launchers (defined in the .cu files; all asynchronous on `stream`).

@@ -166,6 +166,7 @@ __global__ void __launch_bounds__(kConfThreads) prestep_kernel(Shape s, Dev d, l
                                                                const float* __restrict__ logits,
                                                                const __half* __restrict__ k_new,
                                                                const __half* __restrict__ v_new) {
+  pdl_wait();
   const int nconf = s.B * s.SV;
   if (blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(&d.stats->steps, 1ull);
   if ((int)blockIdx.x < nconf) {
@@ -184,11 +185,10 @@ int launch_prestep(const Shape& s, const Dev& d, long long step, const float* lo
       (unsigned)(s.B * s.SV + (units + kAppendUnitsPerBlock - 1) / kAppendUnitsPerBlock);
   const __half* kn = static_cast<const __half*>(k_new);
   const __half* vn = static_cast<const __half*>(v_new);
-  if (s.D == 128)
-    prestep_kernel<128><<<grid, kConfThreads, 0, stream>>>(s, d, step, logits, kn, vn);
-  else
-    prestep_kernel<64><<<grid, kConfThreads, 0, stream>>>(s, d, step, logits, kn, vn);
-  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+  const cudaError_t e =
+      s.D == 128 ? launch_pdl(prestep_kernel<128>, dim3(grid), dim3(kConfThreads), 0, stream, s, d, step, logits, kn, vn)
+                 : launch_pdl(prestep_kernel<64>, dim3(grid), dim3(kConfThreads), 0, stream, s, d, step, logits, kn, vn);
+  return e == cudaSuccess ? 0 : -1;
 }
 
 }  // namespace confkv

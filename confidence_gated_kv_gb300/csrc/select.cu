@@ -107,6 +107,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(Shape s, Dev d, 
   __shared__ int scan_w[kSelWarps];
   __shared__ int s_digit, s_rem, s_dcnt, s_cnt, s_k8, s_evslot, s_evpos;
 
+  pdl_wait();
   const int l = blockIdx.x / s.B, b = blockIdx.x % s.B;
   const size_t lb = lb_index(s, l, b);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -637,9 +638,10 @@ static int launch_select_t(const Shape& s, const Dev& d, long long step, int32_t
       return -1;
     configured = p.bytes;
   }
-  select_kernel<D, kSmemKeys><<<s.L * s.B, kSelThreads, p.bytes, stream>>>(s, d, step, evicted_pos,
-                                                                          n_evicted, p);
-  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+  return launch_pdl(select_kernel<D, kSmemKeys>, dim3(s.L * s.B), dim3(kSelThreads), (size_t)p.bytes,
+                    stream, s, d, step, evicted_pos, n_evicted, p) == cudaSuccess
+             ? 0
+             : -1;
 }
 
 int launch_select(const Shape& s, const Dev& d, long long step, int32_t* evicted_pos,

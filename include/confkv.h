@@ -203,11 +203,15 @@ typedef struct confkv_stats {
 int confkv_get_stats(confkv_ctx* ctx, confkv_stats* out, void* stream);
 
 /* Per-kernel timing with CUDA events on the launching stream.  While enabled,
- * every confkv_step records events around its three kernels (confidence and
- * append / attention / select-compact-requant).  confkv_profile_read
- * synchronises and returns the summed milliseconds of each and the number of
- * steps recorded, then clears them.  At most `max_steps` steps are kept. */
-int confkv_profile_enable(confkv_ctx* ctx, int32_t max_steps);
+ * every `every`-th confkv_step (the first one included) records events
+ * around its three kernels (confidence and append / attention /
+ * select-compact-requant); the others run without events, since each event
+ * record between kernels costs the stream about two microseconds.
+ * confkv_profile_read synchronises and returns the summed milliseconds of
+ * each kernel and the number of steps recorded, then clears them.  At most
+ * `max_steps` recorded steps are kept.  CONFKV_EINVAL if max_steps < 1 or
+ * every < 1. */
+int confkv_profile_enable(confkv_ctx* ctx, int32_t max_steps, int32_t every);
 int confkv_profile_disable(confkv_ctx* ctx);
 int confkv_profile_read(confkv_ctx* ctx, double* ms_prestep, double* ms_attention,
                         double* ms_select, int32_t* steps);

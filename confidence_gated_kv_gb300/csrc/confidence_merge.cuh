@@ -97,7 +97,7 @@ __device__ __forceinline__ void conf_merge_warp(const Shape& s, const Dev& d, in
   const float p1 = expf(tp.z1 - M) / Sv;
   const float c = (float)s.wH * (1.0f - Hhat) + (float)s.wm * (1.0f / (1.0f + expf(-m))) +
                   (float)s.wp * p1;
-  const bool high = (double)c >= s.tau;
+  const bool high = c >= (float)s.tau;   // compared in fp32, the precision of c
   for (int l = lane; l < s.L; l += 32) budget[(size_t)b * s.L + l] = high ? d.n_high[l] : d.n_low[l];
   if (lane == 0) {
     d.cval[b] = (double)c;

@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(Shape s, Dev d, 
 
   // ------------------------------------------------ 1. budget of this layer
   // c was merged once per sequence by the attention kernel of this step.
-  const int N = (d.cval[b] >= s.tau) ? d.n_high[l] : d.n_low[l];
+  const int N = ((float)d.cval[b] >= (float)s.tau) ? d.n_high[l] : d.n_low[l];
 
   // ------------------------------------------------ 2. EMA update, candidate ranges
   const int q8 = (n8 + 3) >> 2;            // INT8 quads (the last one may be partial)

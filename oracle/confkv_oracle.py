@@ -54,7 +54,8 @@ R6  INT8 scales per (sequence, layer, KV head, channel), K and V separately,
 R7  Prefill entries start with a = 0; a new token's EMA starts from 0, so
     after its first update a = (1 - lam) A_self.
 R8  Eviction order: (s ascending, position ascending).
-R9  The budget test is c >= tau, evaluated in float64.
+R9  The budget test is c >= tau, compared in float32 (the pages fix no
+    precision; the kernels form c in fp32), with c itself from float64 sums.
 R10 A duplicated maximum gives p(2) = p(1), m = 0.
 R12 Raw logits (temperature 1), natural logarithm.
 R13 Evicted entries are reported as absolute positions, ascending.
@@ -152,8 +153,9 @@ def confidence(logits, w_H=0.4, w_m=0.3, w_p=0.3) -> Confidence:
 
 def budget(c: float, tau: float, n_high: int, n_low: int) -> int:
     """N = N_high if c >= tau else N_low ([gist-de] Adaptive Budgetauswahl;
-    [rainbus] Algorithm 1 step 4).  N_high is the tight budget."""
-    return int(n_high) if c >= tau else int(n_low)
+    [rainbus] Algorithm 1 step 4).  N_high is the tight budget.  The
+    comparison runs in float32 (R9)."""
+    return int(n_high) if np.float32(c) >= np.float32(tau) else int(n_low)
 
 
 # ----------------------------------------------------------------------------

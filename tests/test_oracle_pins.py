@@ -103,7 +103,16 @@ def test_weights_and_hyperparameters_match_pages():
 
 def test_budget_threshold_is_inclusive():
     assert orc.budget(0.7, 0.7, 10, 20) == 10
-    assert orc.budget(np.nextafter(0.7, 0), 0.7, 10, 20) == 20
+    below = float(np.nextafter(np.float32(0.7), np.float32(0)))
+    assert orc.budget(below, 0.7, 10, 20) == 20
+    above = float(np.nextafter(np.float32(0.7), np.float32(1)))
+    assert orc.budget(above, 0.7, 10, 20) == 10
+
+
+def test_budget_compares_in_float32():
+    # R9: a float64 c that rounds to float32(tau) counts as c >= tau
+    assert orc.budget(float(np.nextafter(0.7, 0)), 0.7, 10, 20) == 10
+    assert orc.budget(0.5, 0.7, 10, 20) == 20 and orc.budget(0.9, 0.7, 10, 20) == 10
 
 
 # ---------------------------------------------------------------- attention

@@ -382,6 +382,98 @@ def run_ours(args):
     return 0
 
 
+# ---------------------------------------------------------------------------
+# --compare: CONF-KV against full KV and a 512-token sliding window on the
+# same kernels (the pages' baselines; they publish the ratios only)
+# ---------------------------------------------------------------------------
+COMPARE_KINDS = ("confkv", "fullkv", "sliding512")
+
+
+def variant_workload(w, kind: str, steps_total: int):
+    """The workload's shape and data under one cache policy.
+
+    confkv      the workload's own budgets, window and weights;
+    fullkv      no eviction (budgets above any cache length) and an FP16
+                window covering the prefill and every generated token, so
+                nothing is ever quantised;
+    sliding512  recency only (alpha = 0) with N_high = N_low = 512, every
+                resident entry inside a 512-token FP16 window."""
+    L = w.L
+    if kind == "confkv":
+        return w
+    if kind == "fullkv":
+        W = (w.T0 + steps_total + 16 + 15) // 16 * 16
+        return w.replace(n_high=(1 << 30,) * L, n_low=(1 << 30,) * L, W=W, cap=16)
+    if kind == "sliding512":
+        return w.replace(n_high=(512,) * L, n_low=(512,) * L, alpha=0.0, W=512)
+    raise ValueError(kind)
+
+
+def run_compare(args):
+    """One JSON line: per-step latency (CUDA events around every step), the
+    step rate and the peak resident KV bytes of each policy over the same
+    trajectory (same prefill, same step inputs), and the ratios the pages
+    quote (p50 latency and throughput of full KV over CONF-KV)."""
+    import numpy as np
+    import torch
+    import confidence_gated_kv_gb300 as ck
+    if not os.path.exists(ck.binding.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    from workload import get_workload, prefill_batch_fast, step_pool_fast
+
+    dev = torch.device("cuda", 0)
+    w0 = get_workload(args.workload)
+    if args.batch:
+        w0 = w0.replace(B=args.batch)
+    gen = args.compare_steps
+    R = args.pool
+    q, kn, vn, lg = step_pool_fast(w0, args.seed, R, dev)
+    stream = torch.cuda.current_stream()
+    res = {}
+    for kind in COMPARE_KINDS:
+        w = variant_workload(w0, kind, args.warmup + gen)
+        cache = ck.Cache(ck.config_from_workload(w), device=dev)
+        k, v = prefill_batch_fast(w0, args.seed, dev)
+        cache.prefill(k, v, [w0.T0] * w0.B)
+        del k, v
+        outs = cache.new_outputs()
+        for s in range(args.warmup):
+            cache.step(q[s % R], kn[s % R], vn[s % R], lg[s % R], outs)
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(gen)]
+        peak = cache.stats()["resident_bytes"]
+        for s in range(gen):
+            j = (args.warmup + s) % R
+            evs[s][0].record(stream)
+            cache.step(q[j], kn[j], vn[j], lg[j], outs)
+            evs[s][1].record(stream)
+            if (s + 1) % 256 == 0 or s == gen - 1:
+                peak = max(peak, cache.stats()["resident_bytes"])   # synchronises
+        torch.cuda.synchronize()
+        ms = np.array([a.elapsed_time(b) for a, b in evs])
+        st = cache.stats()
+        res[kind] = {"p50_ms": float(np.median(ms)), "mean_ms": float(ms.mean()),
+                     "p90_ms": float(np.percentile(ms, 90)), "steps_per_s": 1000.0 / float(ms.mean()),
+                     "peak_kv_bytes": int(peak), "final_resident_entries": int(st["resident"]),
+                     "W": w.W, "budgets": [w.n_high[0], w.n_low[0]], "alpha": w.alpha}
+        del cache, outs
+        torch.cuda.empty_cache()
+    c, f, sl = res["confkv"], res["fullkv"], res["sliding512"]
+    line = {"metric": "CONF-KV vs full KV and sliding-512 on the same kernels, 1 GPU",
+            "workload": w0.name, "batch": w0.B, "prefill": w0.T0, "generated_steps": gen,
+            "warmup": args.warmup, "data": "synthetic", "timing": "CUDA events around every step",
+            "variants": res,
+            "ratios": {"p50_latency_fullkv_over_confkv": f["p50_ms"] / c["p50_ms"],
+                       "throughput_confkv_over_fullkv": f["mean_ms"] / c["mean_ms"],
+                       "throughput_sliding512_over_fullkv": f["mean_ms"] / sl["mean_ms"],
+                       "peak_kv_fullkv_over_confkv": f["peak_kv_bytes"] / max(c["peak_kv_bytes"], 1)},
+            "pages": {"p50_latency_fullkv_over_confkv": 1.8, "throughput_confkv_over_fullkv_batch8": 2.06,
+                      "note": "GPT-2 / Qwen-32B at 2048 generated tokens on the pages' GPU; context only"}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -394,11 +486,16 @@ def main(argv=None):
     ap.add_argument("--pool", type=int, default=16)
     ap.add_argument("--e2e-steps", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--compare", action="store_true",
+                    help="CONF-KV vs full KV vs sliding-512 on the same kernels (one JSON line)")
+    ap.add_argument("--compare-steps", type=int, default=2048, help="generated tokens per policy in --compare")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.compare:
+        return run_compare(args)
     return run_ours(args)
 
 

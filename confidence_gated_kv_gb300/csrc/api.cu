@@ -271,7 +271,12 @@ int confkv_step(confkv_ctx* ctx, const void* q, const void* k_new, const void* v
   // worst case of this step, decided on the host before anything launches
   const long long k_bound = std::max(0LL, ctx->n_bound - ctx->minN);
   const long long n_after = std::min<long long>(ctx->n_bound, ctx->maxN) + 1;
-  const long long n8_after = std::min(ctx->n8_bound + 1, n_after - 1);
+  // a token leaves the FP16 window this step only if position t - W >= 0 for
+  // some sequence; otherwise the INT8 region cannot grow
+  long long t_max = 0;
+  for (int b = 0; b < s.B; ++b) t_max = std::max<long long>(t_max, (long long)ctx->T0[b] + ctx->steps);
+  const long long req_bound = t_max - s.W >= 0 ? 1 : 0;
+  const long long n8_after = std::min(ctx->n8_bound + req_bound, n_after - 1);
   if (k_bound > s.max_evict) return CONFKV_ECAPACITY;
   if (n8_after > s.cap) return CONFKV_ECAPACITY;
   int splits = 0, max_tokens = 0;

@@ -660,15 +660,22 @@ __device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uin
       : "memory");
 }
 
+// Ring positions are copied into the unit header up to this ring size; longer
+// rings (a cache kept entirely in FP16) are read from global memory instead,
+// so the header does not crowd out the K/V stages.
+constexpr int kHdrRingMax = 1024;
+
 // Shared-memory header of one unit (byte offsets).
 struct HeaderLayout {
   int q, sk, sv, pos, bytes;
+  bool pos_in;   // ring positions in the header
   __host__ __device__ HeaderLayout(int G, int D, int WR) {
     q = 0;
     sk = (G * D * 2 + 15) / 16 * 16;
     sv = sk + D * 4;
     pos = sv + D * 4;
-    bytes = (pos + WR * 4 + 127) / 128 * 128;
+    pos_in = WR <= kHdrRingMax;
+    bytes = (pos + (pos_in ? WR * 4 : 0) + 127) / 128 * 128;
   }
 };
 
@@ -791,12 +798,13 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
         if (k >= 2 && !mbar_wait(hempty_bar(hs), (uint32_t)(((k >> 1) - 1) & 1))) { fail(); break; }
         const uint32_t hdst = smem_u32(hbuf + (size_t)hs * hl.bytes);
         const uint32_t qbytes = (uint32_t)(G * D * 2);
-        mbar_arrive_tx(hfull_bar(hs), qbytes + 2u * D * 4 + (uint32_t)s.WR * 4);
+        mbar_arrive_tx(hfull_bar(hs), qbytes + 2u * D * 4 + (hl.pos_in ? (uint32_t)s.WR * 4 : 0u));
         bulk_g2s(hdst + hl.q, reinterpret_cast<const char*>(q) + (lb * s.Hq + (size_t)h * G) * D * 2,
                  qbytes, hfull_bar(hs));
         bulk_g2s(hdst + hl.sk, d.sK + (size_t)u * D, D * 4, hfull_bar(hs));
         bulk_g2s(hdst + hl.sv, d.sV + (size_t)u * D, D * 4, hfull_bar(hs));
-        bulk_g2s(hdst + hl.pos, d.pos + lb * s.S + s.cap, (uint32_t)s.WR * 4, hfull_bar(hs));
+        if (hl.pos_in)
+          bulk_g2s(hdst + hl.pos, d.pos + lb * s.S + s.cap, (uint32_t)s.WR * 4, hfull_bar(hs));
         // K/V stages
         Sched sch;
         sch.init(0, nb8 + nbR, nb8);
@@ -935,7 +943,8 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
     const unsigned char* hdr = hbuf + (size_t)hs * hl.bytes;
     const float* sKh = reinterpret_cast<const float*>(hdr + hl.sk);
     const float* sVh = reinterpret_cast<const float*>(hdr + hl.sv);
-    const int32_t* posh = reinterpret_cast<const int32_t*>(hdr + hl.pos);
+    const int32_t* posh = hl.pos_in ? reinterpret_cast<const int32_t*>(hdr + hl.pos)
+                                    : d.pos + lb * s.S + s.cap;
     float* scg = scg_base + (size_t)hs * G * s.S;
     Sched sch;
     sch.init(0, nb8 + nbR, nb8);

@@ -64,6 +64,34 @@ def test_split_k_cluster_path_and_large_first_eviction():
     assert p.flags.evictions >= 2000 - 600
 
 
+def test_full_kv_long_ring_on_the_persistent_kernel():
+    # full KV: no eviction and an FP16 window longer than every cache, so the
+    # ring (1120 slots) is too long for the unit header and the persistent
+    # kernel reads its positions from global memory; 608 units keep the
+    # persistent launch shape
+    L, B, Hkv = 19, 4, 8
+    w = Workload(name="t_full", B=B, L=L, Hq=16, Hkv=Hkv, d=128, V=1000, T0=40, steps=6,
+                 n_high=(1 << 30,) * L, n_low=(1 << 30,) * L, P=8, W=1100, q_dtype="bf16", cap=16)
+    p = Pair(w, 17, prefill_len=[40, 7, 0, 33])
+    splits, _ = p.cache.attention_plan()
+    assert splits == 1
+    for s in range(6):
+        q, kn, vn, lg = step_inputs(w, 17, s)
+        p.step(q, kn, vn, lg)
+    st = p.cache.stats()
+    assert st["evicted"] == 0 and st["requantised"] == 0
+    assert p.flags.max_out_err <= 2e-3
+
+
+def test_sliding_window_policy_alpha_zero():
+    # recency only: alpha = 0 ranks by position, so every eviction takes the
+    # oldest candidates
+    w = Workload(name="t_slide", B=2, L=2, Hq=8, Hkv=2, d=64, V=800, T0=150, steps=12,
+                 n_high=(64,) * 2, n_low=(64,) * 2, alpha=0.0, P=8, W=64, q_dtype="f16")
+    p = _run(w, 18, 12)
+    assert p.flags.evictions > 0
+
+
 def test_no_eviction_limit_is_plain_attention():
     # budgets above every cache length: nothing is evicted, nothing moves
     w = Workload(name="t_noop", B=2, L=2, Hq=6, Hkv=3, d=64, V=1000, T0=40, steps=12,

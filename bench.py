@@ -331,6 +331,31 @@ def run_ours(args):
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "api": "confkv_step_host", "steps": args.e2e_steps}
 
+    # ------------------------------------------------ CUDA-graph replays (optional)
+    graph = None
+    if args.graph:
+        splits_g, _ = cache.attention_plan()
+        cache.graph_reserve(args.steps)
+        graphs = [cache.capture_step(q[j], kn[j], vn[j], lg[j], outs) for j in range(R)]
+        torch.cuda.synchronize()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        done = 0
+        for s in range(args.steps):
+            graphs[(args.warmup + s) % R].replay()
+            if (s + 1) % 64 == 0:
+                cache.graph_advance(s + 1 - done)
+                done = s + 1
+        g1.record(stream)
+        torch.cuda.synchronize()
+        cache.graph_advance(args.steps - done)
+        cache.graph_release()
+        gms = g0.elapsed_time(g1)
+        graph = {"value": args.steps / (gms / 1000.0), "unit": "steps/s", "ms_per_step": gms / args.steps,
+                 "how": "one captured step per pool entry, replayed; device-side step index",
+                 "ctas_per_unit": splits_g}
+        del graphs
+
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, args.seed)
@@ -372,6 +397,7 @@ def run_ours(args):
             "gpu_launches": 3 * args.steps,
             "clocks": clk,
             "e2e": e2e,
+            "graph": graph,
             "cpu_baseline": cpu,
             "state": {"resident_entries": st["resident"], "resident_kv_bytes": st["resident_bytes"],
                       "evicted_total": st["evicted"], "moved_total": st["moved"]},
@@ -486,6 +512,8 @@ def main(argv=None):
     ap.add_argument("--pool", type=int, default=16)
     ap.add_argument("--e2e-steps", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time CUDA-graph replays of captured steps (extra 'graph' key)")
     ap.add_argument("--compare", action="store_true",
                     help="CONF-KV vs full KV vs sliding-512 on the same kernels (one JSON line)")
     ap.add_argument("--compare-steps", type=int, default=2048, help="generated tokens per policy in --compare")

@@ -87,6 +87,9 @@ def lib() -> ctypes.CDLL:
             "confkv_profile_read": (ctypes.c_int, [vp] + [ctypes.POINTER(ctypes.c_double)] * 3 +
                                     [ctypes.POINTER(i32)]),
             "confkv_attention_plan": (ctypes.c_int, [vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]),
+            "confkv_graph_reserve": (ctypes.c_int, [vp, i64]),
+            "confkv_graph_advance": (ctypes.c_int, [vp, i64]),
+            "confkv_graph_release": (ctypes.c_int, [vp]),
             "confkv_block_offset": (i32, [i32, i32, i32, i32]),
             "confkv_confidence_noalloc": (ctypes.c_int, [vp, i32, i32, ctypes.c_double, ctypes.c_double,
                                                          ctypes.c_double, vp, vp]),
@@ -131,9 +134,22 @@ def _ptr(t) -> Optional[int]:
     return t.data_ptr()
 
 
-def _stream(stream) -> int:
+_raw_stream_fn = None
+
+
+def _stream(stream, device_index: int = -1) -> int:
+    """Raw cudaStream_t of `stream`, or of the current torch stream of the
+    device when None.  The current stream is read through torch's raw-stream
+    accessor when it has one: building a torch Stream object on every decode
+    step costs more host time than the step's three kernel launches."""
+    global _raw_stream_fn
     import torch
     if stream is None:
+        if device_index >= 0:
+            if _raw_stream_fn is None:
+                _raw_stream_fn = getattr(torch._C, "_cuda_getCurrentRawStream", False)
+            if _raw_stream_fn:
+                return _raw_stream_fn(device_index)
         return torch.cuda.current_stream().cuda_stream
     if hasattr(stream, "cuda_stream"):
         return stream.cuda_stream
@@ -182,6 +198,8 @@ class Cache:
         _check(lib().confkv_create(ctypes.byref(cfg), self.workspace.data_ptr(), nbytes, ctypes.byref(h)),
                "confkv_create")
         self._h = h
+        self._fn_step = lib().confkv_step
+        self._dev_index = self.device.index if self.device.index is not None else torch.cuda.current_device()
         self.L, self.B, self.Hq, self.Hkv, self.d, self.V = cfg.L, cfg.B, cfg.Hq, cfg.Hkv, cfg.d, cfg.V
         self.cap = (cfg.cap + 15) // 16 * 16
         self.WR = (cfg.W + 16 + 15) // 16 * 16
@@ -224,10 +242,13 @@ class Cache:
     def step(self, q, k_new, v_new, logits, outs=None, stream=None):
         """One decode step; returns the dict of output tensors."""
         o = self.new_outputs() if outs is None else outs
-        _check(lib().confkv_step(self._h, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(logits),
-                                 _ptr(o["out"]), _ptr(o["budget"]), _ptr(o.get("confidence")),
-                                 _ptr(o["evicted"]), _ptr(o["n_evicted"]), _stream(stream)),
-               "confkv_step")
+        conf = o.get("confidence")
+        st = self._fn_step(self._h, q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), logits.data_ptr(),
+                           o["out"].data_ptr(), o["budget"].data_ptr(),
+                           None if conf is None else conf.data_ptr(), o["evicted"].data_ptr(),
+                           o["n_evicted"].data_ptr(), _stream(stream, self._dev_index))
+        if st != OK:
+            raise ConfkvError(st, "confkv_step")
         return o
 
     def step_host(self, q, k_new, v_new, logits, outs, stream=None):
@@ -312,6 +333,28 @@ class Cache:
         _check(lib().confkv_profile_read(self._h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c),
                                          ctypes.byref(n)), "confkv_profile_read")
         return dict(prestep_ms=a.value, attention_ms=b.value, select_ms=c.value, steps=n.value)
+
+    def graph_reserve(self, steps: int):
+        """Check that `steps` more steps fit and pin one attention launch
+        shape for them (required before capturing a step into a graph)."""
+        _check(lib().confkv_graph_reserve(self._h, int(steps)), "confkv_graph_reserve")
+
+    def graph_advance(self, steps: int):
+        """Account for `steps` executed replays of a captured step."""
+        _check(lib().confkv_graph_advance(self._h, int(steps)), "confkv_graph_advance")
+
+    def graph_release(self):
+        _check(lib().confkv_graph_release(self._h), "confkv_graph_release")
+
+    def capture_step(self, q, k_new, v_new, logits, outs):
+        """Capture one decode step reading these device tensors and writing
+        `outs` into a torch.cuda.CUDAGraph.  Call graph_reserve first; after
+        each g.replay() call graph_advance(1) (or advance several at once)."""
+        import torch
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, capture_error_mode="relaxed"):
+            self.step(q, k_new, v_new, logits, outs)
+        return g
 
     def attention_plan(self):
         sp, sm = ctypes.c_int32(), ctypes.c_int32()

@@ -110,6 +110,8 @@ size_t layout(const Shape& s, char* base, Dev* d, Staging* st) {
   dd.absmax = cv.take<uint32_t>(2 * units * s.D);
   dd.score_ctas = attention_persistent_ctas();
   dd.scores = cv.take<float>((size_t)dd.score_ctas * 2 * s.G * s.S);
+  dd.step_dev = cv.take<long long>(1);
+  dd.sel_done = cv.take<uint32_t>(1);
   Staging sg{};
   sg.q = cv.take<uint16_t>(lbs * s.Hq * s.D);
   sg.k_new = cv.take<uint16_t>(units * s.D);
@@ -148,6 +150,9 @@ struct confkv_ctx {
   int prof_every = 1;        // record every prof_every-th step
   long long prof_tick = 0;   // steps seen while profiling is on
   std::vector<cudaEvent_t> ev;
+  // graph replays: steps reserved and the attention plan pinned for them
+  long long pin_left = 0;
+  int pin_splits = 0, pin_max_tokens = 0;
 };
 
 static int cuda_status(cudaError_t e) { return e == cudaSuccess ? CONFKV_OK : CONFKV_ECUDA; }
@@ -190,6 +195,8 @@ int confkv_create(const confkv_config* cfg, void* workspace, size_t workspace_by
     e = cudaMemcpy(c->d.n_low, c->n_low.data(), s.L * sizeof(int32_t), cudaMemcpyHostToDevice);
   if (e == cudaSuccess) e = cudaMemset(c->d.stats, 0, sizeof(DevStats));
   if (e == cudaSuccess) e = cudaMemset(c->d.status, 0, sizeof(int32_t));
+  if (e == cudaSuccess) e = cudaMemset(c->d.step_dev, 0, sizeof(long long));
+  if (e == cudaSuccess) e = cudaMemset(c->d.sel_done, 0, sizeof(uint32_t));
   if (e != cudaSuccess) {
     delete c;
     return CONFKV_ECUDA;
@@ -222,21 +229,25 @@ int confkv_prefill(confkv_ctx* ctx, const int32_t* prefill_len, const void* k, c
                                   cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess) e = cudaMemsetAsync(ctx->d.stats, 0, sizeof(DevStats), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(ctx->d.status, 0, sizeof(int32_t), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ctx->d.step_dev, 0, sizeof(long long), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ctx->d.sel_done, 0, sizeof(uint32_t), st);
   if (e != cudaSuccess) return CONFKV_ECUDA;
   if (launch_prefill(s, ctx->d, k, v, t_max, ctx->T0.data(), st) != 0) return CONFKV_ECUDA;
   // the host copy of T0 is pageable: make sure it has been consumed
   if (cudaStreamSynchronize(st) != cudaSuccess) return CONFKV_ECUDA;
   ctx->prefilled = true;
   ctx->steps = 0;
+  ctx->pin_left = 0;
   ctx->n_bound = tmax0;
   ctx->n8_bound = std::max<long long>(0, tmax0 - s.W);
   return CONFKV_OK;
 }
 
-// Launch shape of the attention kernel for the current bounds.
-static int plan_attention(const confkv_ctx* ctx, int* splits_out, int* max_tokens_out) {
+// Launch shape of the attention kernel for an INT8 bound.
+static int plan_attention_for(const confkv_ctx* ctx, long long n8_bound, int* splits_out,
+                              int* max_tokens_out) {
   const Shape& s = ctx->s;
-  const int max_tokens = (int)align_up((size_t)ctx->n8_bound, 16) + s.WR;
+  const int max_tokens = (int)align_up((size_t)n8_bound, 16) + s.WR;
   const long long units = (long long)s.L * s.B * s.Hkv;
   const int nbT = max_tokens / 16;
   int splits = 1;
@@ -247,6 +258,36 @@ static int plan_attention(const confkv_ctx* ctx, int* splits_out, int* max_token
   if (attention_smem_bytes(s, splits, max_tokens) > attention_max_smem()) return CONFKV_ECAPACITY;
   *splits_out = splits;
   *max_tokens_out = max_tokens;
+  return CONFKV_OK;
+}
+
+// Launch shape for the current bounds (the pinned one while steps are reserved).
+static int plan_attention(const confkv_ctx* ctx, int* splits_out, int* max_tokens_out) {
+  if (ctx->pin_left > 0) {
+    *splits_out = ctx->pin_splits;
+    *max_tokens_out = ctx->pin_max_tokens;
+    return CONFKV_OK;
+  }
+  return plan_attention_for(ctx, ctx->n8_bound, splits_out, max_tokens_out);
+}
+
+// Checks of one step taken with host bounds (steps, n_bound, n8_bound) and the
+// bounds after it: worst cases, decided on the host before anything launches.
+static int step_bounds(const confkv_ctx* ctx, long long steps, long long n_bound, long long n8_bound,
+                       long long* n_after, long long* n8_after) {
+  const Shape& s = ctx->s;
+  const long long k_bound = std::max(0LL, n_bound - ctx->minN);
+  *n_after = std::min<long long>(n_bound, ctx->maxN) + 1;
+  // a token leaves the FP16 window this step only if position t - W >= 0 for
+  // some sequence; otherwise the INT8 region cannot grow
+  long long t_max = 0;
+  for (int b = 0; b < s.B; ++b) t_max = std::max<long long>(t_max, (long long)ctx->T0[b] + steps);
+  const long long req_bound = t_max - s.W >= 0 ? 1 : 0;
+  *n8_after = std::min(n8_bound + req_bound, *n_after - 1);
+  if (k_bound > s.max_evict) return CONFKV_ECAPACITY;
+  if (*n8_after > s.cap) return CONFKV_ECAPACITY;
+  // positions stay in int32
+  if (t_max >= (1LL << 31) - 1) return CONFKV_ECAPACITY;
   return CONFKV_OK;
 }
 
@@ -268,43 +309,90 @@ int confkv_step(confkv_ctx* ctx, const void* q, const void* k_new, const void* v
   if (!q || !k_new || !v_new || !logits || !out || !budget || !evicted_pos || !n_evicted)
     return CONFKV_EINVAL;
   const Shape& s = ctx->s;
-  // worst case of this step, decided on the host before anything launches
-  const long long k_bound = std::max(0LL, ctx->n_bound - ctx->minN);
-  const long long n_after = std::min<long long>(ctx->n_bound, ctx->maxN) + 1;
-  // a token leaves the FP16 window this step only if position t - W >= 0 for
-  // some sequence; otherwise the INT8 region cannot grow
-  long long t_max = 0;
-  for (int b = 0; b < s.B; ++b) t_max = std::max<long long>(t_max, (long long)ctx->T0[b] + ctx->steps);
-  const long long req_bound = t_max - s.W >= 0 ? 1 : 0;
-  const long long n8_after = std::min(ctx->n8_bound + req_bound, n_after - 1);
-  if (k_bound > s.max_evict) return CONFKV_ECAPACITY;
-  if (n8_after > s.cap) return CONFKV_ECAPACITY;
-  int splits = 0, max_tokens = 0;
-  const int pr = plan_attention(ctx, &splits, &max_tokens);
-  if (pr != CONFKV_OK) return pr;
-  // positions stay in int32
-  for (int b = 0; b < s.B; ++b)
-    if ((long long)ctx->T0[b] + ctx->steps >= (1LL << 31) - 1) return CONFKV_ECAPACITY;
-
   cudaStream_t st = as_stream(stream);
-  const bool prof = ctx->prof_on && ctx->prof_count < ctx->prof_max &&
+  // Under stream capture nothing runs now: the launches go into a graph
+  // whose replays the caller accounts for with confkv_graph_advance, inside
+  // a reservation made with confkv_graph_reserve.
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return CONFKV_ECUDA;
+  const bool capturing = cs != cudaStreamCaptureStatusNone;
+  if (capturing && ctx->pin_left <= 0) return CONFKV_ESTATE;
+  long long n_after = 0, n8_after = 0;
+  int r = step_bounds(ctx, ctx->steps, ctx->n_bound, ctx->n8_bound, &n_after, &n8_after);
+  if (r != CONFKV_OK) return r;
+  int splits = 0, max_tokens = 0;
+  r = plan_attention(ctx, &splits, &max_tokens);
+  if (r != CONFKV_OK) return r;
+
+  const bool prof = !capturing && ctx->prof_on && ctx->prof_count < ctx->prof_max &&
                     (ctx->prof_tick++ % ctx->prof_every) == 0;
   cudaEvent_t* ev = prof ? &ctx->ev[4 * ctx->prof_count] : nullptr;
   if (prof) cudaEventRecord(ev[0], st);
-  if (launch_prestep(s, ctx->d, ctx->steps, logits, k_new, v_new, st) != 0) return CONFKV_ECUDA;
+  // inside a graph reservation every step (captured or not) takes its index
+  // from the device counter, which the reservation set and each step advances
+  const long long step_arg = (capturing || ctx->pin_left > 0) ? -1 : ctx->steps;
+  if (launch_prestep(s, ctx->d, step_arg, logits, k_new, v_new, st) != 0) return CONFKV_ECUDA;
   if (prof) cudaEventRecord(ev[1], st);
   if (launch_attention(s, ctx->d, q, out, budget, confidence, splits, max_tokens, st) != 0)
     return CONFKV_ECUDA;
   if (prof) cudaEventRecord(ev[2], st);
-  if (launch_select(s, ctx->d, ctx->steps, evicted_pos, n_evicted, st) != 0)
-    return CONFKV_ECUDA;
+  if (launch_select(s, ctx->d, step_arg, evicted_pos, n_evicted, st) != 0) return CONFKV_ECUDA;
   if (prof) {
     cudaEventRecord(ev[3], st);
     ctx->prof_count++;
   }
-  ctx->steps++;
-  ctx->n_bound = n_after;
-  ctx->n8_bound = n8_after;
+  if (!capturing) {
+    ctx->steps++;
+    ctx->n_bound = n_after;
+    ctx->n8_bound = n8_after;
+    if (ctx->pin_left > 0) ctx->pin_left--;
+  }
+  return CONFKV_OK;
+}
+
+int confkv_graph_reserve(confkv_ctx* ctx, int64_t steps) {
+  if (!ctx || steps < 1) return CONFKV_EINVAL;
+  if (!ctx->prefilled) return CONFKV_ESTATE;
+  long long n_bound = ctx->n_bound, n8_bound = ctx->n8_bound, n8_max = n8_bound;
+  for (long long i = 0; i < steps; ++i) {
+    long long na = 0, n8a = 0;
+    const int r = step_bounds(ctx, ctx->steps + i, n_bound, n8_bound, &na, &n8a);
+    if (r != CONFKV_OK) return r;
+    n8_max = std::max(n8_max, n8_bound);
+    n_bound = na;
+    n8_bound = n8a;
+  }
+  int splits = 0, max_tokens = 0;
+  const int r = plan_attention_for(ctx, n8_max, &splits, &max_tokens);
+  if (r != CONFKV_OK) return r;
+  // the device step counter starts from the host's count (steps outside a
+  // reservation pass their index as an argument and leave it alone)
+  if (cudaMemcpy(ctx->d.step_dev, &ctx->steps, sizeof(long long), cudaMemcpyHostToDevice) != cudaSuccess)
+    return CONFKV_ECUDA;
+  ctx->pin_left = steps;
+  ctx->pin_splits = splits;
+  ctx->pin_max_tokens = max_tokens;
+  return CONFKV_OK;
+}
+
+int confkv_graph_advance(confkv_ctx* ctx, int64_t steps) {
+  if (!ctx || steps < 0) return CONFKV_EINVAL;
+  if (steps > ctx->pin_left) return CONFKV_ESTATE;
+  for (long long i = 0; i < steps; ++i) {
+    long long na = 0, n8a = 0;
+    const int r = step_bounds(ctx, ctx->steps, ctx->n_bound, ctx->n8_bound, &na, &n8a);
+    if (r != CONFKV_OK) return r;   // cannot happen inside a reservation
+    ctx->steps++;
+    ctx->n_bound = na;
+    ctx->n8_bound = n8a;
+  }
+  ctx->pin_left -= steps;
+  return CONFKV_OK;
+}
+
+int confkv_graph_release(confkv_ctx* ctx) {
+  if (!ctx) return CONFKV_EINVAL;
+  ctx->pin_left = 0;
   return CONFKV_OK;
 }
 
@@ -317,6 +405,9 @@ int confkv_step_host(confkv_ctx* ctx, const void* q, const void* k_new, const vo
   const Shape& s = ctx->s;
   const Staging& g = ctx->st;
   cudaStream_t st = as_stream(stream);
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) return CONFKV_ECUDA;
+  if (cs != cudaStreamCaptureStatusNone) return CONFKV_ESTATE;   // host copies stay outside graphs
   const size_t lbs = (size_t)s.L * s.B;
   const size_t nq = lbs * s.Hq * s.D * 2, nkv = lbs * s.Hkv * s.D * 2;
   cudaError_t e = cudaMemcpyAsync(g.q, q, nq, cudaMemcpyHostToDevice, st);
@@ -475,6 +566,7 @@ int confkv_import_unit(confkv_ctx* ctx, int32_t b, int32_t l, const confkv_unit_
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return CONFKV_ECUDA;
   ctx->prefilled = true;
+  ctx->pin_left = 0;   // bounds may have grown: a pinned plan no longer holds
   ctx->n_bound = std::max<long long>(ctx->n_bound, (long long)in->n8 + in->nR);
   ctx->n8_bound = std::max<long long>(ctx->n8_bound, in->n8);
   return CONFKV_OK;
@@ -495,6 +587,8 @@ int confkv_set_clock(confkv_ctx* ctx, const int32_t* prefill_len, int64_t steps,
   ctx->steps = steps;
   cudaStream_t st = as_stream(stream);
   cudaError_t e = cudaMemcpyAsync(ctx->d.T0, ctx->T0.data(), ctx->s.B * 4, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(ctx->d.step_dev, &ctx->steps, sizeof(long long), cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   return cuda_status(e);
 }

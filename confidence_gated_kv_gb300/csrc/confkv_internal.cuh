@@ -127,6 +127,8 @@ struct Dev {
   uint32_t* absmax;                // [2][l][b][kvh][D] prefill scratch
   float* scores;                   // [persistent CTAs][2][G][S] attention score scratch
   int score_ctas;                  // persistent attention CTAs the score scratch holds
+  long long* step_dev;             // decode steps done since prefill (read by prestep and select)
+  uint32_t* sel_done;              // select CTAs finished in the current step (0 between steps)
 };
 
 // Status bits written by kernels (never trap; the host reads them lazily).
@@ -181,6 +183,9 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 // ---------------------------------------------------------------------------
 int launch_prefill(const Shape& s, const Dev& d, const void* k, const void* v, long long t_max,
                    const int32_t* T0_host, cudaStream_t stream);
+// step: the index of this decode step, or -1 for a step that takes it from
+// d.step_dev (a step captured into a graph, and every step while replays are
+// reserved); the select kernel of such a step advances d.step_dev.
 int launch_prestep(const Shape& s, const Dev& d, long long step, const float* logits,
                    const void* k_new, const void* v_new, cudaStream_t stream);
 int launch_attention(const Shape& s, const Dev& d, const void* q, float* out, int32_t* budget,

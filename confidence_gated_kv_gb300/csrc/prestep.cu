@@ -114,8 +114,8 @@ __device__ void conf_block(const Shape& s, const Dev& d, const float* __restrict
 // t mod WR.  One warp per unit, four units in flight per warp: lane i writes
 // the 8 bytes of K that hold channels 16(i/4) + 2(i%4) + {0, 1, 8, 9} of the
 // interleaved FP16 block (one aligned store) and V channels i, i + 32, ...
-template <int D>
-__device__ void append_units(const Shape& s, const Dev& d, long long step, int u0, int u1,
+template <int D, bool kDevStep>
+__device__ void append_units(const Shape& s, const Dev& d, long long step_arg, int u0, int u1,
                              const __half* __restrict__ k_new, const __half* __restrict__ v_new) {
   constexpr int kU = 4;
   constexpr int kV = D / 32;
@@ -139,6 +139,9 @@ __device__ void append_units(const Shape& s, const Dev& d, long long step, int u
 #pragma unroll
     for (int i = 0; i < kV; ++i) vx[j][i] = vn[lane + 32 * i];
   }
+  // a step inside a graph reservation reads the step index from the device
+  // (after the payload loads are in flight); other steps take the argument
+  const long long step = kDevStep ? __ldcg(d.step_dev) : step_arg;
 #pragma unroll
   for (int j = 0; j < kU; ++j) {
     const int u = u0 + warp + j * nwarps;
@@ -161,7 +164,7 @@ __device__ void append_units(const Shape& s, const Dev& d, long long step, int u
 
 constexpr int kAppendUnitsPerBlock = 4 * (kConfThreads / 32);
 
-template <int D>
+template <int D, bool kDevStep>
 __global__ void __launch_bounds__(kConfThreads) prestep_kernel(Shape s, Dev d, long long step,
                                                                const float* __restrict__ logits,
                                                                const __half* __restrict__ k_new,
@@ -174,7 +177,7 @@ __global__ void __launch_bounds__(kConfThreads) prestep_kernel(Shape s, Dev d, l
   } else {
     const int units = s.L * s.B * s.Hkv;
     const int u0 = ((int)blockIdx.x - nconf) * kAppendUnitsPerBlock;
-    append_units<D>(s, d, step, u0, min(units, u0 + kAppendUnitsPerBlock), k_new, v_new);
+    append_units<D, kDevStep>(s, d, step, u0, min(units, u0 + kAppendUnitsPerBlock), k_new, v_new);
   }
 }
 
@@ -185,9 +188,14 @@ int launch_prestep(const Shape& s, const Dev& d, long long step, const float* lo
       (unsigned)(s.B * s.SV + (units + kAppendUnitsPerBlock - 1) / kAppendUnitsPerBlock);
   const __half* kn = static_cast<const __half*>(k_new);
   const __half* vn = static_cast<const __half*>(v_new);
-  const cudaError_t e =
-      s.D == 128 ? launch_pdl(prestep_kernel<128>, dim3(grid), dim3(kConfThreads), 0, stream, s, d, step, logits, kn, vn)
-                 : launch_pdl(prestep_kernel<64>, dim3(grid), dim3(kConfThreads), 0, stream, s, d, step, logits, kn, vn);
+  const dim3 g(grid), blk(kConfThreads);
+  cudaError_t e;
+  if (step >= 0)
+    e = s.D == 128 ? launch_pdl(prestep_kernel<128, false>, g, blk, 0, stream, s, d, step, logits, kn, vn)
+                   : launch_pdl(prestep_kernel<64, false>, g, blk, 0, stream, s, d, step, logits, kn, vn);
+  else
+    e = s.D == 128 ? launch_pdl(prestep_kernel<128, true>, g, blk, 0, stream, s, d, step, logits, kn, vn)
+                   : launch_pdl(prestep_kernel<64, true>, g, blk, 0, stream, s, d, step, logits, kn, vn);
   return e == cudaSuccess ? 0 : -1;
 }
 

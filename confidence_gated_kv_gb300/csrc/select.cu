@@ -92,8 +92,8 @@ __device__ __forceinline__ void hist_find(const int* hist, int rem, int lane, in
   }
 }
 
-template <int D, bool kSmemKeys>
-__global__ void __launch_bounds__(kSelThreads, 4) select_kernel(Shape s, Dev d, long long step,
+template <int D, bool kSmemKeys, bool kDevStep>
+__global__ void __launch_bounds__(kSelThreads, 4) select_kernel(Shape s, Dev d, long long step_arg,
                                                              int32_t* __restrict__ evicted_out,
                                                              int32_t* __restrict__ nevict_out,
                                                              SelSmem sm) {
@@ -108,6 +108,8 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(Shape s, Dev d, 
   __shared__ int s_digit, s_rem, s_dcnt, s_cnt, s_k8, s_evslot, s_evpos;
 
   pdl_wait();
+  // a step inside a graph reservation reads the step index from the device
+  const long long step = kDevStep ? __ldcg(d.step_dev) : step_arg;
   const int l = blockIdx.x / s.B, b = blockIdx.x % s.B;
   const size_t lb = lb_index(s, l, b);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -605,6 +607,16 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(Shape s, Dev d, 
     atomicAdd(&d.stats->attn_bytes, attn);
     atomicAdd(&d.stats->step_bytes, step_b);
     if (blockIdx.x == 0) atomicAdd(&d.stats->steps, 1ull);
+    if (kDevStep) {
+      // the last CTA to finish advances the step index (every CTA has read it
+      // before its own increment of the counter)
+      __threadfence();
+      if (atomicAdd(d.sel_done, 1u) == gridDim.x - 1) {
+        *d.sel_done = 0u;
+        *d.step_dev = step + 1;
+        __threadfence();
+      }
+    }
   }
 }
 
@@ -628,20 +640,27 @@ static SelSmem plan_select(const Shape& s) {
   return p;
 }
 
-template <int D, bool kSmemKeys>
+template <int D, bool kSmemKeys, bool kDevStep>
 static int launch_select_t(const Shape& s, const Dev& d, long long step, int32_t* evicted_pos,
                            int32_t* n_evicted, const SelSmem& p, cudaStream_t stream) {
   static int configured = 48 * 1024;
   if (p.bytes > configured) {
-    if (cudaFuncSetAttribute(select_kernel<D, kSmemKeys>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             p.bytes) != cudaSuccess)
+    if (cudaFuncSetAttribute(select_kernel<D, kSmemKeys, kDevStep>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, p.bytes) != cudaSuccess)
       return -1;
     configured = p.bytes;
   }
-  return launch_pdl(select_kernel<D, kSmemKeys>, dim3(s.L * s.B), dim3(kSelThreads), (size_t)p.bytes,
-                    stream, s, d, step, evicted_pos, n_evicted, p) == cudaSuccess
+  return launch_pdl(select_kernel<D, kSmemKeys, kDevStep>, dim3(s.L * s.B), dim3(kSelThreads),
+                    (size_t)p.bytes, stream, s, d, step, evicted_pos, n_evicted, p) == cudaSuccess
              ? 0
              : -1;
+}
+
+template <int D, bool kSmemKeys>
+static int launch_select_s(const Shape& s, const Dev& d, long long step, int32_t* evicted_pos,
+                           int32_t* n_evicted, const SelSmem& p, cudaStream_t stream) {
+  return step >= 0 ? launch_select_t<D, kSmemKeys, false>(s, d, step, evicted_pos, n_evicted, p, stream)
+                   : launch_select_t<D, kSmemKeys, true>(s, d, step, evicted_pos, n_evicted, p, stream);
 }
 
 int launch_select(const Shape& s, const Dev& d, long long step, int32_t* evicted_pos,
@@ -649,10 +668,10 @@ int launch_select(const Shape& s, const Dev& d, long long step, int32_t* evicted
   const SelSmem p = plan_select(s);
   const bool smem_keys = p.off_key >= 0;
   if (s.D == 128)
-    return smem_keys ? launch_select_t<128, true>(s, d, step, evicted_pos, n_evicted, p, stream)
-                     : launch_select_t<128, false>(s, d, step, evicted_pos, n_evicted, p, stream);
-  return smem_keys ? launch_select_t<64, true>(s, d, step, evicted_pos, n_evicted, p, stream)
-                   : launch_select_t<64, false>(s, d, step, evicted_pos, n_evicted, p, stream);
+    return smem_keys ? launch_select_s<128, true>(s, d, step, evicted_pos, n_evicted, p, stream)
+                     : launch_select_s<128, false>(s, d, step, evicted_pos, n_evicted, p, stream);
+  return smem_keys ? launch_select_s<64, true>(s, d, step, evicted_pos, n_evicted, p, stream)
+                   : launch_select_s<64, false>(s, d, step, evicted_pos, n_evicted, p, stream);
 }
 
 }  // namespace confkv

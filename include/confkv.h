@@ -151,6 +151,31 @@ int confkv_step_host(confkv_ctx* ctx, const void* q, const void* k_new, const vo
                      const float* logits, float* out, int32_t* budget, float* confidence,
                      int32_t* evicted_pos, int32_t* n_evicted, void* stream);
 
+/* CUDA graphs.  The step index lives in device memory, so the three kernels
+ * of a confkv_step captured into a CUDA graph (stream capture on `stream`)
+ * replay correctly step after step.  The host still keeps worst-case bounds
+ * (capacity, eviction rows, attention launch shape), so replays go inside a
+ * reservation:
+ *   confkv_graph_reserve(ctx, n)  checks that n more steps fit under the
+ *       worst-case bounds and pins one attention launch shape valid for all
+ *       of them.  CONFKV_ECAPACITY if they do not fit, CONFKV_ESTATE before
+ *       prefill, CONFKV_EINVAL if n < 1.
+ *   confkv_step under capture then records a step without running it and
+ *       without advancing the host state; under capture without a
+ *       reservation it returns CONFKV_ESTATE.  confkv_step_host is never
+ *       captured (CONFKV_ESTATE).
+ *   confkv_graph_advance(ctx, k)  accounts for k executed replays (k at most
+ *       the steps left in the reservation, else CONFKV_ESTATE).  Plain
+ *       confkv_step calls inside a reservation use the pinned shape and
+ *       count against it as well.
+ *   confkv_graph_release(ctx)  drops the reservation (prefill and
+ *       confkv_import_unit drop it too).
+ * The pages have no counterpart of these calls: they serve callers that put
+ * the cache manager into their own decode graph. */
+int confkv_graph_reserve(confkv_ctx* ctx, int64_t steps);
+int confkv_graph_advance(confkv_ctx* ctx, int64_t steps);
+int confkv_graph_release(confkv_ctx* ctx);
+
 /* Cache of one (sequence b, layer l) in a plain host layout.  Caller-owned
  * buffers sized for cap INT8 entries and W + 16 FP16 entries:
  *   pos8[cap], ema8[cap], k8/v8[cap][Hkv][d] int8 codes,

@@ -116,9 +116,14 @@ class Pair:
             e = compare_unit(self.cache.export_unit(b, l), self.oracle.states[l][b], "unit b%d l%d" % (b, l))
             self.flags.max_ema_err = max(self.flags.max_ema_err, e)
 
-    def step(self, q, kn, vn, lg, check_state=True):
+    def step(self, q, kn, vn, lg, check_state=True, gpu_step=None):
+        """One step on both sides; `gpu_step(q, kn, vn, lg)` replaces the
+        plain cache.step call (graph replays) and returns the output dict."""
         w = self.w
-        o = self.cache.step(q.cuda(), kn.cuda(), vn.cuda(), lg.cuda())
+        if gpu_step is None:
+            o = self.cache.step(q.cuda(), kn.cuda(), vn.cuda(), lg.cuda())
+        else:
+            o = gpu_step(q, kn, vn, lg)
         torch.cuda.synchronize()
         res = self.oracle.step(q, kn, vn, lg)
         self.flags.steps += 1

@@ -92,6 +92,57 @@ def test_sliding_window_policy_alpha_zero():
     assert p.flags.evictions > 0
 
 
+def test_captured_step_replays_match_the_oracle():
+    # one step captured into a CUDA graph, replayed with new inputs copied
+    # into the captured buffers: the device-side step index advances, the
+    # host accounts for each replay inside a reservation
+    w = Workload(name="t_graph", B=2, L=2, Hq=10, Hkv=2, d=128, V=3000, T0=260, steps=12,
+                 n_high=(40, 30), n_low=(100, 90), P=8, W=32, q_dtype="bf16",
+                 heavy_count=5, heavy_factor=3.0)
+    p = Pair(w, 19)
+    q0, kn0, vn0, lg0 = step_inputs(w, 19, 0)
+    p.step(q0, kn0, vn0, lg0)                       # plain step first
+    sq, skn, svn, slg = q0.cuda(), kn0.cuda(), vn0.cuda(), lg0.cuda()
+    outs = p.cache.new_outputs()
+    state = {}
+
+    def capture():
+        p.cache.graph_reserve(w.steps)
+        state["g"] = p.cache.capture_step(sq, skn, svn, slg, outs)
+
+    def replay(q, kn, vn, lg):
+        if p.cache._h is not None and "g" not in state:
+            capture()
+        sq.copy_(q); skn.copy_(kn); svn.copy_(vn); slg.copy_(lg)
+        state["g"].replay()
+        p.cache.graph_advance(1)
+        return outs
+
+    capture()
+    for s in range(1, w.steps):
+        q, kn, vn, lg = step_inputs(w, 19, s)
+        if s % 4 == 3:
+            lg = confident_logits(w.V, w.B, 19000 + s)
+        before = p.flags.ties + p.flags.budget
+        p.step(q, kn, vn, lg, gpu_step=replay)
+        if p.flags.ties + p.flags.budget != before:
+            state.pop("g")                          # a resync drops the reservation
+    assert p.flags.evictions > 0
+    assert p.flags.max_out_err <= 2e-3
+
+
+def test_capture_without_reservation_is_refused():
+    w = Workload(name="t_graph2", B=1, L=1, Hq=4, Hkv=2, d=64, V=500, T0=40, steps=2,
+                 n_high=(32,), n_low=(48,), P=4, W=16, q_dtype="f16")
+    p = Pair(w, 20)
+    q, kn, vn, lg = (x.cuda() for x in step_inputs(w, 20, 0))
+    outs = p.cache.new_outputs()
+    with pytest.raises(ck.ConfkvError):
+        p.cache.capture_step(q, kn, vn, lg, outs)
+    st = p.cache.stats()
+    assert st["steps"] == 0 and st["device_status"] == 0
+
+
 def test_no_eviction_limit_is_plain_attention():
     # budgets above every cache length: nothing is evicted, nothing moves
     w = Workload(name="t_noop", B=2, L=2, Hq=6, Hkv=3, d=64, V=1000, T0=40, steps=12,

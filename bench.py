@@ -249,7 +249,7 @@ def run_ours(args):
     if args.batch:
         w = w.replace(B=args.batch)
     seed = args.seed + 7919 * rank
-    cfg = ck.config_from_workload(w)
+    cfg = ck.config_from_workload(w, compaction=1 if args.compaction == "ordered" else 0)
     cache = ck.Cache(cfg, device=dev)
     k, v = prefill_batch_fast(w, seed, dev)
     cache.prefill(k, v, [w.T0] * w.B)
@@ -376,7 +376,8 @@ def run_ours(args):
             "vs_baseline": None,
             "dtype": "fp16/int8 storage, fp16 tensor-core products, fp32 accumulate",
             "data": "synthetic",
-            "config": {"workload": w.name, "global_batch": w.B * ws, "seq_len": w.T0, "layers": w.L,
+            "config": {"workload": w.name, "compaction": args.compaction, "global_batch": w.B * ws,
+                       "seq_len": w.T0, "layers": w.L,
                        "heads": [w.Hq, w.Hkv], "head_dim": w.d, "vocab": w.V,
                        "budgets": [w.n_high[0], w.n_low[0]], "P": w.P, "W": w.W,
                        "parallelism": "replicas (dp%d over sequences)" % ws,
@@ -512,6 +513,8 @@ def main(argv=None):
     ap.add_argument("--pool", type=int, default=16)
     ap.add_argument("--e2e-steps", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--compaction", default="tailfill", choices=["tailfill", "ordered"],
+                    help="INT8 compaction: tail fill (default) or the order-preserving ablation")
     ap.add_argument("--graph", action="store_true",
                     help="also time CUDA-graph replays of captured steps (extra 'graph' key)")
     ap.add_argument("--compare", action="store_true",

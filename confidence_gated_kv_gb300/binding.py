@@ -35,7 +35,10 @@ class Config(ctypes.Structure):
         ("tau", ctypes.c_double), ("w_H", ctypes.c_double), ("w_m", ctypes.c_double),
         ("w_p", ctypes.c_double), ("alpha", ctypes.c_float), ("lam", ctypes.c_float),
         ("n_high", ctypes.POINTER(ctypes.c_int32)), ("n_low", ctypes.POINTER(ctypes.c_int32)),
+        ("compaction", ctypes.c_int32),
     ]
+
+COMPACT_TAIL_FILL, COMPACT_ORDERED = 0, 1
 
 
 class UnitHost(ctypes.Structure):
@@ -157,23 +160,24 @@ def _stream(stream, device_index: int = -1) -> int:
 
 
 def make_config(L, Hq, Hkv, d, V, B, cap, W, P, n_high, n_low, q_dtype="f16", tau=0.7, alpha=0.65,
-                lam=0.9, w_H=0.4, w_m=0.3, w_p=0.3, max_evict=0):
+                lam=0.9, w_H=0.4, w_m=0.3, w_p=0.3, max_evict=0, compaction=COMPACT_TAIL_FILL):
     """Build a Config; keeps the budget arrays alive on the returned object."""
     nh = (ctypes.c_int32 * L)(*[int(x) for x in n_high])
     nl = (ctypes.c_int32 * L)(*[int(x) for x in n_low])
     c = Config(L=L, Hq=Hq, Hkv=Hkv, d=d, V=V, B=B, cap=cap, W=W, P=P,
                q_dtype=Q_BF16 if q_dtype in ("bf16", Q_BF16) else Q_FP16,
                max_evict=max_evict, tau=tau, w_H=w_H, w_m=w_m, w_p=w_p, alpha=alpha, lam=lam,
-               n_high=nh, n_low=nl)
+               n_high=nh, n_low=nl, compaction=int(compaction))
     c._keep = (nh, nl)
     return c
 
 
-def config_from_workload(w, B: Optional[int] = None, cap: Optional[int] = None, max_evict: int = 0):
+def config_from_workload(w, B: Optional[int] = None, cap: Optional[int] = None, max_evict: int = 0,
+                         compaction: int = COMPACT_TAIL_FILL):
     return make_config(L=w.L, Hq=w.Hq, Hkv=w.Hkv, d=w.d, V=w.V, B=w.B if B is None else B,
                        cap=w.capacity if cap is None else cap, W=w.W, P=w.P, n_high=w.n_high,
                        n_low=w.n_low, q_dtype=w.q_dtype, tau=w.tau, alpha=w.alpha, lam=w.lam,
-                       w_H=w.w_H, w_m=w.w_m, w_p=w.w_p, max_evict=max_evict)
+                       w_H=w.w_H, w_m=w.w_m, w_p=w.w_p, max_evict=max_evict, compaction=compaction)
 
 
 def workspace_bytes(cfg: Config) -> int:

@@ -45,6 +45,7 @@ bool valid_config(const confkv_config* c) {
   if (c->L < 1 || c->B < 1 || c->Hq < 1 || c->Hkv < 1 || c->V < 2 || c->W < 1 || c->P < 0)
     return false;
   if ((long long)c->V > 4096LL * kMaxSV) return false;   // vocabulary chunks of <= 4096 logits
+  if (c->compaction != CONFKV_COMPACT_TAIL_FILL && c->compaction != CONFKV_COMPACT_ORDERED) return false;
   if (c->Hq % c->Hkv != 0 || c->Hq / c->Hkv > kMaxG) return false;
   if (c->d != 64 && c->d != 128) return false;
   if (c->cap < 16 || c->max_evict < 0) return false;
@@ -80,6 +81,7 @@ Shape make_shape(const confkv_config* c) {
   s.max_evict = c->max_evict > 0 ? c->max_evict : s.cap + s.WR;
   s.tau = c->tau; s.wH = c->w_H; s.wm = c->w_m; s.wp = c->w_p;
   s.alpha = c->alpha; s.lam = c->lam;
+  s.compaction = c->compaction;
   return s;
 }
 

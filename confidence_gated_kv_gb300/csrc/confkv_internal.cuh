@@ -108,6 +108,7 @@ struct Shape {
   int max_evict;             // rows of evicted_pos per (l, b)
   double tau, wH, wm, wp;     // confidence weights and threshold (float64 math)
   float alpha, lam;           // rank weight and EMA decay (float32 math)
+  int compaction;             // 0 tail fill, 1 order preserving (ablation)
 };
 
 struct Dev {

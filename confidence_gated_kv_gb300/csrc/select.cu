@@ -52,8 +52,114 @@ struct SelSmem {
   int off_bm8;       // [cap / 32] u32: evicted INT8 slots
   int off_key;       // [S] u32 keys, then the compaction lists (keys in shared memory only)
   int off_pos;       // [S] i32 candidate positions, INT_MAX elsewhere (keys in shared memory only)
+  int off_wpre;      // [cap / 32 + 1] i32 evicted slots before each bitmap word (ordered compaction)
+  int off_stage;     // [warps][Hkv][64] u32 one token per warp in flight (ordered compaction)
   int bytes;
 };
+
+constexpr int kOrdWin = kSelWarps;   // ordered compaction: slots per window, one per warp
+
+// Order-preserving compaction of the INT8 region (the ablation of tail fill):
+// every survivor at slot i moves to i - (evicted slots below i).  Windows of
+// kOrdWin slots in increasing order; warp w stages slot a + w in shared
+// memory, the block synchronises, then every warp stores.  A destination is
+// always below its source, so a window's stores never touch a later
+// window's sources; inside a window a store can hit another warp's source,
+// hence the barrier between the loads and the stores.  Returns the moves.
+template <int D>
+__device__ __forceinline__ int ordered_compaction(const Shape& s, const Dev& d, size_t u0, int n8,
+                                                  const uint32_t* bm8, int* wpre, uint32_t* stage,
+                                                  int32_t* pos, float* ema, int* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nw = (n8 + 31) >> 5;
+  constexpr int kV = D / 32;
+  // exclusive prefix of the evicted counts per bitmap word, and the first hole
+  int base = 0, first = INT_MAX;
+  for (int w0 = 0; w0 < nw; w0 += kSelThreads) {
+    const int w = w0 + threadIdx.x;
+    const uint32_t bits = w < nw ? bm8[w] : 0u;
+    const int c = __popc(bits);
+    if (bits) first = min(first, w * 32 + __ffs(bits) - 1);
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    __syncthreads();
+    if (lane == 31) red[warp] = incl;
+    __syncthreads();
+    int off = base, tot = 0;
+    for (int ww = 0; ww < kSelWarps; ++ww) {
+      if (ww < warp) off += red[ww];
+      tot += red[ww];
+    }
+    if (w < nw) wpre[w] = off + incl - c;
+    base += tot;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) first = min(first, __shfl_xor_sync(0xffffffffu, first, o));
+  __syncthreads();
+  if (lane == 0) red[warp] = first;
+  __syncthreads();
+  for (int ww = 0; ww < kSelWarps; ++ww) first = min(first, red[ww]);
+  if (first >= n8) return 0;
+  const size_t ustride8 = (size_t)s.cstride * D;
+  const int kc0 = 16 * (lane >> 2) + 2 * (lane & 3);
+  uint32_t* mine = stage + (size_t)warp * s.Hkv * 64;
+  int moved = 0;
+  for (int a = first; a < n8; a += kOrdWin) {
+    const int i = a + warp;
+    int dst = i;
+    int32_t mp = 0;
+    float me = 0.f;
+    if (i < n8 && !((bm8[i >> 5] >> (i & 31)) & 1u))
+      dst = i - (wpre[i >> 5] + __popc(bm8[i >> 5] & ((1u << (i & 31)) - 1u)));
+    const bool mv = dst != i;
+    if (mv) {
+      const size_t sblk = (size_t)(i >> 4) * 16 * D;
+      for (int h = 0; h < s.Hkv; ++h) {
+        const uint8_t* k8u = d.k8 + (u0 + h) * ustride8 + sblk;
+        const uint8_t* v8u = d.v8 + (u0 + h) * ustride8 + sblk;
+        if (lane < D / 4) mine[h * 64 + lane] = *reinterpret_cast<const uint32_t*>(k8u + k8_offset(D, i & 15, kc0));
+        uint32_t vb = 0u;
+#pragma unroll
+        for (int c = 0; c < kV; ++c) vb |= (uint32_t)v8u[v8_offset(D, i & 15, lane + 32 * c)] << (8 * c);
+        mine[h * 64 + 32 + lane] = vb;
+      }
+      mp = pos[i];
+      me = ema[i];
+      ++moved;
+    }
+    __syncthreads();
+    if (mv) {
+      const size_t dblk = (size_t)(dst >> 4) * 16 * D;
+      for (int h = 0; h < s.Hkv; ++h) {
+        uint8_t* k8u = d.k8 + (u0 + h) * ustride8 + dblk;
+        uint8_t* v8u = d.v8 + (u0 + h) * ustride8 + dblk;
+        if (lane < D / 4) *reinterpret_cast<uint32_t*>(k8u + k8_offset(D, dst & 15, kc0)) = mine[h * 64 + lane];
+        const uint32_t vb = mine[h * 64 + 32 + lane];
+#pragma unroll
+        for (int c = 0; c < kV; ++c) v8u[v8_offset(D, dst & 15, lane + 32 * c)] = (uint8_t)(vb >> (8 * c));
+      }
+      if (lane == 0) {
+        pos[dst] = mp;
+        ema[dst] = me;
+      }
+    }
+  }
+  __syncthreads();
+  // every lane of a moving warp counted the move once per warp: lane 0 reports
+  int m = lane == 0 ? moved : 0;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m += __shfl_xor_sync(0xffffffffu, m, o);
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  int total = 0;
+  for (int ww = 0; ww < kSelWarps; ++ww) total += red[ww];
+  __syncthreads();
+  return total;
+}
 
 // Stored byte of code = clamp(rint(x / s), -127, 127): the code + 128.
 __device__ __forceinline__ uint32_t quant_code_sel(float x, float s) {
@@ -92,7 +198,7 @@ __device__ __forceinline__ void hist_find(const int* hist, int rem, int lane, in
   }
 }
 
-template <int D, bool kSmemKeys, bool kDevStep>
+template <int D, bool kSmemKeys, bool kDevStep, bool kOrdered>
 __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(Shape s, Dev d, long long step_arg,
                                                              int32_t* __restrict__ evicted_out,
                                                              int32_t* __restrict__ nevict_out,
@@ -426,6 +532,16 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(Shape s, Dev d, 
   // ------------------------------------------------ 5. compaction and requantisation
   const int n8p = n8 - k8;
   int moves = 0;
+  constexpr bool ordered = kOrdered;   // order-preserving compaction (ablation instances only)
+  if (ordered && k8 > 0) {
+    if (k == 1) {
+      if (threadIdx.x == 0) bm8[s_evslot >> 5] |= 1u << (s_evslot & 31);
+      __syncthreads();
+    }
+    moves = ordered_compaction<D>(s, d, unit_index(s, l, b, 0), n8, bm8,
+                                  reinterpret_cast<int*>(dsm + sm.off_wpre),
+                                  reinterpret_cast<uint32_t*>(dsm + sm.off_stage), pos, ema, red_i[0]);
+  }
   const size_t u0 = unit_index(s, l, b, 0);
   const size_t ustride8 = (size_t)s.cstride * D;        // INT8 bytes per unit
   const size_t ustride16 = (size_t)WR * D * 2;          // FP16 ring bytes per unit
@@ -441,7 +557,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(Shape s, Dev d, 
   const int kc0 = 16 * kw + 2 * kt;
   constexpr int kVPerLane = D / 32;
 
-  if (k > 1 && k8 > 0) {
+  if (!ordered && k > 1 && k8 > 0) {
     // ---------------------------------------------- tail fill: holes < n8p <- survivors >= n8p
     uint32_t* hole = KEY;                 // [moves]
     uint32_t* mover = KEY + (S >> 1);     // [moves]
@@ -522,7 +638,7 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(Shape s, Dev d, 
   // one eviction from the INT8 region: move slot n8 - 1 into the hole (same
   // lanes as the requantisation below, which may rewrite slot n8 - 1)
   const int dst1 = s_evslot, src1 = n8 - 1;
-  const bool move1 = k == 1 && k8 == 1 && dst1 < src1;
+  const bool move1 = !ordered && k == 1 && k8 == 1 && dst1 < src1;
   if (move1) moves = 1;
   const char* k16b = reinterpret_cast<const char*>(d.k16);
   const char* v16b = reinterpret_cast<const char*>(d.v16);
@@ -627,6 +743,13 @@ static SelSmem plan_select(const Shape& s) {
   off += (size_t)kPosWords * 4;
   p.off_bm8 = (int)off;
   off += ((size_t)(s.cap / 32) * 4 + 15) & ~(size_t)15;
+  p.off_wpre = p.off_stage = -1;
+  if (s.compaction == 1) {
+    p.off_wpre = (int)off;
+    off += ((size_t)(s.cap / 32 + 1) * 4 + 15) & ~(size_t)15;
+    p.off_stage = (int)off;
+    off += (size_t)kSelWarps * s.Hkv * 64 * 4;
+  }
   const size_t keys = (size_t)s.S * 4;
   if (off + 2 * keys <= kSelSmemKeysMax) {
     p.off_key = (int)off;
@@ -640,27 +763,35 @@ static SelSmem plan_select(const Shape& s) {
   return p;
 }
 
-template <int D, bool kSmemKeys, bool kDevStep>
+template <int D, bool kSmemKeys, bool kDevStep, bool kOrdered>
 static int launch_select_t(const Shape& s, const Dev& d, long long step, int32_t* evicted_pos,
                            int32_t* n_evicted, const SelSmem& p, cudaStream_t stream) {
   static int configured = 48 * 1024;
   if (p.bytes > configured) {
-    if (cudaFuncSetAttribute(select_kernel<D, kSmemKeys, kDevStep>,
+    if (cudaFuncSetAttribute(select_kernel<D, kSmemKeys, kDevStep, kOrdered>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, p.bytes) != cudaSuccess)
       return -1;
     configured = p.bytes;
   }
-  return launch_pdl(select_kernel<D, kSmemKeys, kDevStep>, dim3(s.L * s.B), dim3(kSelThreads),
+  return launch_pdl(select_kernel<D, kSmemKeys, kDevStep, kOrdered>, dim3(s.L * s.B), dim3(kSelThreads),
                     (size_t)p.bytes, stream, s, d, step, evicted_pos, n_evicted, p) == cudaSuccess
              ? 0
              : -1;
 }
 
+template <int D, bool kSmemKeys, bool kDevStep>
+static int launch_select_o(const Shape& s, const Dev& d, long long step, int32_t* evicted_pos,
+                           int32_t* n_evicted, const SelSmem& p, cudaStream_t stream) {
+  return s.compaction == 1
+             ? launch_select_t<D, kSmemKeys, kDevStep, true>(s, d, step, evicted_pos, n_evicted, p, stream)
+             : launch_select_t<D, kSmemKeys, kDevStep, false>(s, d, step, evicted_pos, n_evicted, p, stream);
+}
+
 template <int D, bool kSmemKeys>
 static int launch_select_s(const Shape& s, const Dev& d, long long step, int32_t* evicted_pos,
                            int32_t* n_evicted, const SelSmem& p, cudaStream_t stream) {
-  return step >= 0 ? launch_select_t<D, kSmemKeys, false>(s, d, step, evicted_pos, n_evicted, p, stream)
-                   : launch_select_t<D, kSmemKeys, true>(s, d, step, evicted_pos, n_evicted, p, stream);
+  return step >= 0 ? launch_select_o<D, kSmemKeys, false>(s, d, step, evicted_pos, n_evicted, p, stream)
+                   : launch_select_o<D, kSmemKeys, true>(s, d, step, evicted_pos, n_evicted, p, stream);
 }
 
 int launch_select(const Shape& s, const Dev& d, long long step, int32_t* evicted_pos,

@@ -78,14 +78,24 @@ typedef struct confkv_config {
   const int32_t* n_low;       /* host [L]: loose budget per layer (c < tau);
                                  per-layer values give the pyramidal variant
                                  ([gist-de] Systemintegration) */
+  int32_t compaction;         /* CONFKV_COMPACT_TAIL_FILL (0, default): each
+                                 evicted INT8 slot below the new length takes a
+                                 survivor from above it (at most k moves);
+                                 CONFKV_COMPACT_ORDERED (1): survivors keep
+                                 position order (every survivor above the first
+                                 hole moves), the contiguous compaction of
+                                 [gist-de] Systemintegration, kept as an
+                                 ablation of the layout */
 } confkv_config;
+
+enum { CONFKV_COMPACT_TAIL_FILL = 0, CONFKV_COMPACT_ORDERED = 1 };
 
 typedef struct confkv_ctx confkv_ctx;
 
 /* Bytes of device workspace the context needs (state + scratch).  Returns
  * CONFKV_EINVAL for an invalid configuration: d not 64/128, Hq % Hkv != 0,
  * Hq / Hkv > 8, V < 2 or V > 4096 * 1024, some budget < P or < 1, cap < 16,
- * W < 1. */
+ * W < 1, compaction not 0 or 1. */
 int confkv_workspace_bytes(const confkv_config* cfg, size_t* bytes);
 
 /* Create a context over `workspace` (device memory, >= the size above, 256-byte

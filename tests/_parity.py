@@ -91,7 +91,8 @@ def check_evictions(gpu_ev: np.ndarray, r: orc.UnitStepResult, where: str) -> bo
 class Pair:
     """CUDA cache + oracle driven by the same inputs."""
 
-    def __init__(self, w, seed: int, prefill_len=None, cap=None, max_evict=0, k=None, v=None):
+    def __init__(self, w, seed: int, prefill_len=None, cap=None, max_evict=0, k=None, v=None,
+                 compaction=0):
         self.w = w
         self.seed = seed
         self.prm = orc.Params.from_workload(w)
@@ -101,7 +102,7 @@ class Pair:
             k, v = prefill_batch(w, seed, "cpu", T0=max(self.T0) if self.T0 else 0)
         self.oracle = orc.Oracle(self.prm)
         self.oracle.prefill(k, v, self.T0)
-        self.cache = ck.Cache(ck.config_from_workload(w, cap=cap, max_evict=max_evict))
+        self.cache = ck.Cache(ck.config_from_workload(w, cap=cap, max_evict=max_evict, compaction=compaction))
         self.cache.prefill(k.cuda(), v.cuda(), self.T0)
         self.flags = Flags()
 

@@ -143,6 +143,26 @@ def test_capture_without_reservation_is_refused():
     assert st["steps"] == 0 and st["device_status"] == 0
 
 
+def test_order_preserving_compaction_ablation():
+    # the ablation layout: survivors keep position order in the INT8 region
+    # (every survivor above the first hole moves); same results as tail fill
+    w = Workload(name="t_ord", B=3, L=2, Hq=10, Hkv=2, d=128, V=3000, T0=300, steps=24,
+                 n_high=(40, 30), n_low=(120, 90), P=8, W=32, q_dtype="bf16",
+                 heavy_count=5, heavy_factor=3.0)
+    p = Pair(w, 21, prefill_len=[300, 17, 150], compaction=ck.binding.COMPACT_ORDERED)
+    for s in range(w.steps):
+        q, kn, vn, lg = step_inputs(w, 21, s)
+        if s % 5 == 4:
+            lg = confident_logits(w.V, w.B, 21000 + s)
+        p.step(q, kn, vn, lg)
+        for b in range(w.B):
+            for l in range(w.L):
+                pos8 = p.cache.export_unit(b, l)["pos8"]
+                assert np.all(np.diff(pos8) > 0), "INT8 slots out of position order (b%d l%d)" % (b, l)
+    assert p.flags.evictions > 0
+    assert p.cache.stats()["moved"] > 0
+
+
 def test_no_eviction_limit_is_plain_attention():
     # budgets above every cache length: nothing is evicted, nothing moves
     w = Workload(name="t_noop", B=2, L=2, Hq=6, Hkv=3, d=64, V=1000, T0=40, steps=12,

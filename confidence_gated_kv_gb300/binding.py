@@ -58,6 +58,7 @@ class Stats(ctypes.Structure):
         ("requantised", ctypes.c_int64), ("attn_bytes", ctypes.c_double),
         ("step_bytes", ctypes.c_double), ("resident", ctypes.c_int64),
         ("resident_bytes", ctypes.c_int64), ("device_status", ctypes.c_int32),
+        ("host_h2d_bytes", ctypes.c_int64), ("host_d2h_bytes", ctypes.c_int64),
     ]
 
 

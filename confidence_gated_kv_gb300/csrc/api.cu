@@ -146,6 +146,7 @@ struct confkv_ctx {
   long long n_bound = 0;    // max resident entries of any (l, b), new token excluded
   long long n8_bound = 0;   // max INT8 entries of any (l, b)
   int minN = 0, maxN = 0;
+  long long host_h2d = 0, host_d2h = 0;   // bytes of the last confkv_step_host
   // profiling
   bool prof_on = false;
   int prof_max = 0, prof_count = 0;
@@ -418,6 +419,9 @@ int confkv_step_host(confkv_ctx* ctx, const void* q, const void* k_new, const vo
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(g.logits, logits, (size_t)s.B * s.V * 4, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return CONFKV_ECUDA;
+  // no row of evicted positions can hold more than this step's eviction bound
+  const long long k_bound =
+      std::min<long long>(s.max_evict, std::max(0LL, ctx->n_bound - ctx->minN));
   const int r = confkv_step(ctx, g.q, g.k_new, g.v_new, g.logits, g.out, g.budget,
                             confidence ? g.conf : nullptr, g.evicted, g.nevict, stream);
   if (r != CONFKV_OK) return r;
@@ -425,10 +429,15 @@ int confkv_step_host(confkv_ctx* ctx, const void* q, const void* k_new, const vo
   if (e == cudaSuccess) e = cudaMemcpyAsync(budget, g.budget, lbs * 4, cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess && confidence)
     e = cudaMemcpyAsync(confidence, g.conf, (size_t)s.B * 4, cudaMemcpyDeviceToHost, st);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(evicted_pos, g.evicted, lbs * s.max_evict * 4, cudaMemcpyDeviceToHost, st);
+  // the first k_bound entries of every row: the rest is never written
+  if (e == cudaSuccess && k_bound > 0)
+    e = cudaMemcpy2DAsync(evicted_pos, (size_t)s.max_evict * 4, g.evicted, (size_t)s.max_evict * 4,
+                          (size_t)k_bound * 4, lbs, cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(n_evicted, g.nevict, lbs * 4, cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  ctx->host_h2d = (long long)(nq + 2 * nkv + (size_t)s.B * s.V * 4);
+  ctx->host_d2h = (long long)(lbs * s.Hq * s.D * 4 + lbs * 4 + (confidence ? (size_t)s.B * 4 : 0) +
+                              lbs * (size_t)k_bound * 4 + lbs * 4);
   return cuda_status(e);
 }
 
@@ -627,6 +636,8 @@ int confkv_get_stats(confkv_ctx* ctx, confkv_stats* out, void* stream) {
   out->resident = res;
   out->resident_bytes = res_bytes;
   out->device_status = status;
+  out->host_h2d_bytes = ctx->host_h2d;
+  out->host_d2h_bytes = ctx->host_d2h;
   return status ? CONFKV_EDEVICE : CONFKV_OK;
 }
 

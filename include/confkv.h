@@ -155,7 +155,9 @@ int confkv_step(confkv_ctx* ctx, const void* q, const void* k_new, const void* v
  * confkv_step with HOST buffers (same shapes): copies the inputs to device
  * staging buffers inside the workspace, runs the step and copies the outputs
  * back, all on `stream`, then synchronises the stream.  Pinned host memory
- * makes the copies asynchronous DMA.  confidence may be NULL.
+ * makes the copies asynchronous DMA.  confidence may be NULL.  Of each row
+ * of evicted_pos only the entries the step could write are copied back (as
+ * many as its worst-case eviction count); the rest of the row is untouched.
  */
 int confkv_step_host(confkv_ctx* ctx, const void* q, const void* k_new, const void* v_new,
                      const float* logits, float* out, int32_t* budget, float* confidence,
@@ -231,6 +233,8 @@ typedef struct confkv_stats {
   int64_t resident;          /* cache entries resident now, all units */
   int64_t resident_bytes;    /* K/V bytes resident now at stored widths */
   int32_t device_status;     /* raw device status bits (0 = ok) */
+  int64_t host_h2d_bytes;    /* bytes the last confkv_step_host copied to the device */
+  int64_t host_d2h_bytes;    /* bytes the last confkv_step_host copied back */
 } confkv_stats;
 
 /* Read the counters and the device status word (synchronises `stream`).

@@ -147,6 +147,10 @@ struct confkv_ctx {
   long long n8_bound = 0;   // max INT8 entries of any (l, b)
   int minN = 0, maxN = 0;
   long long host_h2d = 0, host_d2h = 0;   // bytes of the last confkv_step_host
+  // confkv_step_host: a second stream copies the attention output back while
+  // the select kernel runs (created on first use)
+  cudaStream_t aux = nullptr;
+  cudaEvent_t ev_attn = nullptr, ev_aux = nullptr;
   // profiling
   bool prof_on = false;
   int prof_max = 0, prof_count = 0;
@@ -212,6 +216,9 @@ int confkv_create(const confkv_config* cfg, void* workspace, size_t workspace_by
 void confkv_destroy(confkv_ctx* ctx) {
   if (!ctx) return;
   for (cudaEvent_t e : ctx->ev) cudaEventDestroy(e);
+  if (ctx->ev_attn) cudaEventDestroy(ctx->ev_attn);
+  if (ctx->ev_aux) cudaEventDestroy(ctx->ev_aux);
+  if (ctx->aux) cudaStreamDestroy(ctx->aux);
   delete ctx;
 }
 
@@ -304,9 +311,22 @@ int confkv_attention_plan(confkv_ctx* ctx, int32_t* splits, int32_t* smem_bytes)
   return CONFKV_OK;
 }
 
+static int step_impl(confkv_ctx* ctx, const void* q, const void* k_new, const void* v_new,
+                     const float* logits, float* out, int32_t* budget, float* confidence,
+                     int32_t* evicted_pos, int32_t* n_evicted, void* stream, cudaEvent_t after_attention);
+
 int confkv_step(confkv_ctx* ctx, const void* q, const void* k_new, const void* v_new,
                 const float* logits, float* out, int32_t* budget, float* confidence,
                 int32_t* evicted_pos, int32_t* n_evicted, void* stream) {
+  return step_impl(ctx, q, k_new, v_new, logits, out, budget, confidence, evicted_pos, n_evicted, stream,
+                   nullptr);
+}
+
+// after_attention: recorded on `stream` once the attention kernel (the last
+// writer of `out`) has been launched, when not null
+static int step_impl(confkv_ctx* ctx, const void* q, const void* k_new, const void* v_new,
+                     const float* logits, float* out, int32_t* budget, float* confidence,
+                     int32_t* evicted_pos, int32_t* n_evicted, void* stream, cudaEvent_t after_attention) {
   if (!ctx) return CONFKV_EINVAL;
   if (!ctx->prefilled) return CONFKV_ESTATE;
   if (!q || !k_new || !v_new || !logits || !out || !budget || !evicted_pos || !n_evicted)
@@ -339,6 +359,7 @@ int confkv_step(confkv_ctx* ctx, const void* q, const void* k_new, const void* v
   if (launch_attention(s, ctx->d, q, out, budget, confidence, splits, max_tokens, st) != 0)
     return CONFKV_ECUDA;
   if (prof) cudaEventRecord(ev[2], st);
+  if (after_attention && cudaEventRecord(after_attention, st) != cudaSuccess) return CONFKV_ECUDA;
   if (launch_select(s, ctx->d, step_arg, evicted_pos, n_evicted, st) != 0) return CONFKV_ECUDA;
   if (prof) {
     cudaEventRecord(ev[3], st);
@@ -422,10 +443,20 @@ int confkv_step_host(confkv_ctx* ctx, const void* q, const void* k_new, const vo
   // no row of evicted positions can hold more than this step's eviction bound
   const long long k_bound =
       std::min<long long>(s.max_evict, std::max(0LL, ctx->n_bound - ctx->minN));
-  const int r = confkv_step(ctx, g.q, g.k_new, g.v_new, g.logits, g.out, g.budget,
-                            confidence ? g.conf : nullptr, g.evicted, g.nevict, stream);
+  if (!ctx->aux) {
+    if (cudaStreamCreateWithFlags(&ctx->aux, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ctx->ev_attn, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ctx->ev_aux, cudaEventDisableTiming) != cudaSuccess)
+      return CONFKV_ECUDA;
+  }
+  const int r = step_impl(ctx, g.q, g.k_new, g.v_new, g.logits, g.out, g.budget,
+                          confidence ? g.conf : nullptr, g.evicted, g.nevict, stream, ctx->ev_attn);
   if (r != CONFKV_OK) return r;
-  e = cudaMemcpyAsync(out, g.out, lbs * s.Hq * s.D * 4, cudaMemcpyDeviceToHost, st);
+  // the attention output is final once the attention kernel is done: copy it
+  // back on the second stream while the select kernel runs
+  e = cudaStreamWaitEvent(ctx->aux, ctx->ev_attn, 0);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(out, g.out, lbs * s.Hq * s.D * 4, cudaMemcpyDeviceToHost, ctx->aux);
+  if (e == cudaSuccess) e = cudaEventRecord(ctx->ev_aux, ctx->aux);
   if (e == cudaSuccess) e = cudaMemcpyAsync(budget, g.budget, lbs * 4, cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess && confidence)
     e = cudaMemcpyAsync(confidence, g.conf, (size_t)s.B * 4, cudaMemcpyDeviceToHost, st);
@@ -434,6 +465,7 @@ int confkv_step_host(confkv_ctx* ctx, const void* q, const void* k_new, const vo
     e = cudaMemcpy2DAsync(evicted_pos, (size_t)s.max_evict * 4, g.evicted, (size_t)s.max_evict * 4,
                           (size_t)k_bound * 4, lbs, cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(n_evicted, g.nevict, lbs * 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(st, ctx->ev_aux, 0);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   ctx->host_h2d = (long long)(nq + 2 * nkv + (size_t)s.B * s.V * 4);
   ctx->host_d2h = (long long)(lbs * s.Hq * s.D * 4 + lbs * 4 + (confidence ? (size_t)s.B * 4 : 0) +

@@ -154,8 +154,11 @@ int confkv_step(confkv_ctx* ctx, const void* q, const void* k_new, const void* v
 /*
  * confkv_step with HOST buffers (same shapes): copies the inputs to device
  * staging buffers inside the workspace, runs the step and copies the outputs
- * back, all on `stream`, then synchronises the stream.  Pinned host memory
- * makes the copies asynchronous DMA.  confidence may be NULL.  Of each row
+ * back, then synchronises.  The attention output is copied back on a second,
+ * library-owned stream (created on the first call) while the last kernel of
+ * the step runs; everything else runs on `stream`, and the call returns
+ * after both are done.  Pinned host memory makes the copies asynchronous
+ * DMA.  confidence may be NULL.  Of each row
  * of evicted_pos only the entries the step could write are copied back (as
  * many as its worst-case eviction count); the rest of the row is untouched.
  */

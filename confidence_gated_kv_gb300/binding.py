@@ -39,6 +39,7 @@ class Config(ctypes.Structure):
     ]
 
 COMPACT_TAIL_FILL, COMPACT_ORDERED = 0, 1
+STATUS_CAPACITY, STATUS_EVICT_BOUND, STATUS_BAD_COUNT, STATUS_TIMEOUT = 1, 2, 4, 8
 
 
 class UnitHost(ctypes.Structure):
@@ -94,6 +95,7 @@ def lib() -> ctypes.CDLL:
             "confkv_graph_reserve": (ctypes.c_int, [vp, i64]),
             "confkv_graph_advance": (ctypes.c_int, [vp, i64]),
             "confkv_graph_release": (ctypes.c_int, [vp]),
+            "confkv_selftest_timeout": (ctypes.c_int, [vp, vp]),
             "confkv_block_offset": (i32, [i32, i32, i32, i32]),
             "confkv_confidence_noalloc": (ctypes.c_int, [vp, i32, i32, ctypes.c_double, ctypes.c_double,
                                                          ctypes.c_double, vp, vp]),
@@ -347,6 +349,10 @@ class Cache:
     def graph_advance(self, steps: int):
         """Account for `steps` executed replays of a captured step."""
         _check(lib().confkv_graph_advance(self._h, int(steps)), "confkv_graph_advance")
+
+    def selftest_timeout(self, stream=None):
+        """Run the bounded-wait self-test: sets the time-out status bit."""
+        _check(lib().confkv_selftest_timeout(self._h, _stream(stream)), "confkv_selftest_timeout")
 
     def graph_release(self):
         _check(lib().confkv_graph_release(self._h), "confkv_graph_release")

@@ -414,6 +414,11 @@ int confkv_graph_advance(confkv_ctx* ctx, int64_t steps) {
   return CONFKV_OK;
 }
 
+int confkv_selftest_timeout(confkv_ctx* ctx, void* stream) {
+  if (!ctx) return CONFKV_EINVAL;
+  return launch_selftest_timeout(ctx->d, as_stream(stream)) == 0 ? CONFKV_OK : CONFKV_ECUDA;
+}
+
 int confkv_graph_release(confkv_ctx* ctx) {
   if (!ctx) return CONFKV_EINVAL;
   ctx->pin_left = 0;

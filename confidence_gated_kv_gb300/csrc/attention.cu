@@ -1083,6 +1083,31 @@ static int num_sms() {
 
 int attention_persistent_ctas() { return 2 * num_sms(); }
 
+// Self-test of the bounded-wait path: one CTA waits on an mbarrier that no
+// thread ever arrives on, with a short poll limit, then reports the time-out
+// through the device status word exactly as the decode kernels do.  Nothing
+// faults and the context stays usable.
+__global__ void selftest_wait_kernel(Dev d, long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    bool done = false;
+    for (long long i = 0; i < limit && !done; ++i) done = mbar_try_wait(b, 0);
+    if (!done) atomicOr(d.status, kStatusTimeout);
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];\n" ::"r"(b) : "memory");
+  }
+}
+
+int launch_selftest_timeout(const Dev& d, cudaStream_t stream) {
+  selftest_wait_kernel<<<1, 32, 0, stream>>>(d, 4096);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
 template <int D>
 static int launch_d(const Shape& s, const Dev& d, const void* q, float* out, int32_t* budget,
                     float* conf_out, int splits, int max_tokens, cudaStream_t stream) {

@@ -196,5 +196,6 @@ int launch_select(const Shape& s, const Dev& d, long long step, int32_t* evicted
 int attention_smem_bytes(const Shape& s, int splits, int max_tokens);
 int attention_max_smem();
 int attention_persistent_ctas();   // persistent CTAs per launch (2 per SM)
+int launch_selftest_timeout(const Dev& d, cudaStream_t stream);
 
 }  // namespace confkv

@@ -188,6 +188,14 @@ int confkv_step_host(confkv_ctx* ctx, const void* q, const void* k_new, const vo
  * The pages have no counterpart of these calls: they serve callers that put
  * the cache manager into their own decode graph. */
 int confkv_graph_reserve(confkv_ctx* ctx, int64_t steps);
+/* Self-test of failure detection: launches one CTA that waits on an mbarrier
+ * nothing ever arrives on, with the decode kernels' polling loop but a short
+ * limit (4096 polls).  The wait runs out and sets the time-out bit
+ * (CONFKV_STATUS_TIMEOUT) of the device status word, which the next
+ * confkv_get_stats reports as CONFKV_EDEVICE; nothing faults and the context
+ * stays usable (confkv_prefill clears the word).  Asynchronous on `stream`.
+ * The pages have no counterpart: it tests this library's own bounded waits. */
+int confkv_selftest_timeout(confkv_ctx* ctx, void* stream);
 int confkv_graph_advance(confkv_ctx* ctx, int64_t steps);
 int confkv_graph_release(confkv_ctx* ctx);
 
@@ -225,6 +233,14 @@ int confkv_import_unit(confkv_ctx* ctx, int32_t b, int32_t l, const confkv_unit_
  * prefill.  confkv_set_clock restores it with a checkpoint. */
 int confkv_get_clock(confkv_ctx* ctx, int32_t* prefill_len, int64_t* steps);
 int confkv_set_clock(confkv_ctx* ctx, const int32_t* prefill_len, int64_t steps, void* stream);
+
+/* Bits of the device status word (confkv_stats.device_status). */
+enum {
+  CONFKV_STATUS_CAPACITY = 1,     /* an INT8 region would have overflowed cap */
+  CONFKV_STATUS_EVICT_BOUND = 2,  /* more evictions than evicted_pos rows hold */
+  CONFKV_STATUS_BAD_COUNT = 4,    /* eviction count differs from n - N */
+  CONFKV_STATUS_TIMEOUT = 8       /* a bounded wait inside a kernel gave up */
+};
 
 typedef struct confkv_stats {
   int64_t steps;             /* steps since prefill */

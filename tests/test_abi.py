@@ -119,3 +119,15 @@ def test_null_handles_are_rejected():
     assert L.confkv_prefill(None, None, None, None, 0, None) == binding.EINVAL
     assert L.confkv_get_stats(None, None, None) == binding.EINVAL
     L.confkv_destroy(None)
+
+
+def test_status_bits_match_the_kernels():
+    import re
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    hdr = open(os.path.join(root, "include", "confkv.h")).read()
+    internal = open(os.path.join(root, "confidence_gated_kv_gb300", "csrc", "confkv_internal.cuh")).read()
+    pub = {m.group(1): int(m.group(2)) for m in re.finditer(r"CONFKV_STATUS_(\w+) = (\d+)", hdr)}
+    dev = {m.group(1): int(m.group(2)) for m in re.finditer(r"kStatus(\w+) = (\d+)", internal)}
+    want = {"CAPACITY": "Capacity", "EVICT_BOUND": "EvictBound", "BAD_COUNT": "BadCount", "TIMEOUT": "Timeout"}
+    for k, v in want.items():
+        assert pub[k] == dev[v]

@@ -163,6 +163,26 @@ def test_order_preserving_compaction_ablation():
     assert p.cache.stats()["moved"] > 0
 
 
+def test_bounded_wait_reports_a_timeout_and_the_context_survives():
+    # failure detection without a fault: a wait that nothing satisfies runs
+    # out, the status word says so, and the context keeps working
+    w = Workload(name="t_to", B=1, L=1, Hq=4, Hkv=2, d=64, V=500, T0=40, steps=2,
+                 n_high=(32,), n_low=(48,), P=4, W=16, q_dtype="f16")
+    p = Pair(w, 24)
+    p.cache.selftest_timeout()
+    st = p.cache.stats(check=False)
+    assert st["device_status"] & ck.binding.STATUS_TIMEOUT
+    with pytest.raises(ck.ConfkvError):
+        p.cache.stats()
+    # prefill clears the word; the context still steps correctly
+    from workload import prefill_batch
+    k, v = prefill_batch(w, 24, "cpu")
+    p.cache.prefill(k.cuda(), v.cuda(), [w.T0])
+    assert p.cache.stats()["device_status"] == 0
+    q, kn, vn, lg = step_inputs(w, 24, 0)
+    p.step(q, kn, vn, lg)
+
+
 def test_no_eviction_limit_is_plain_attention():
     # budgets above every cache length: nothing is evicted, nothing moves
     w = Workload(name="t_noop", B=2, L=2, Hq=6, Hkv=3, d=64, V=1000, T0=40, steps=12,

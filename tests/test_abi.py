@@ -89,7 +89,7 @@ def _cfg(**kw):
 @pytest.mark.parametrize("bad", [
     dict(d=96), dict(Hq=6, Hkv=4), dict(Hq=18, Hkv=2), dict(V=1), dict(V=4096 * 1024 + 1), dict(W=0),
     dict(n_high=[4, 40]), dict(n_low=[80, 0]), dict(cap=8), dict(L=0), dict(B=0),
-    dict(alpha=1.5), dict(lam=-0.1), dict(q_dtype=7), dict(P=-1),
+    dict(alpha=1.5), dict(lam=-0.1), dict(q_dtype=7), dict(P=-1), dict(compaction=2),
 ])
 def test_invalid_configurations_rejected(bad):
     c = _cfg(**bad)
@@ -131,3 +131,8 @@ def test_status_bits_match_the_kernels():
     want = {"CAPACITY": "Capacity", "EVICT_BOUND": "EvictBound", "BAD_COUNT": "BadCount", "TIMEOUT": "Timeout"}
     for k, v in want.items():
         assert pub[k] == dev[v]
+
+
+def test_both_compaction_layouts_are_valid():
+    for c in (binding.COMPACT_TAIL_FILL, binding.COMPACT_ORDERED):
+        assert ck.workspace_bytes(_cfg(compaction=c)) > 0

@@ -113,22 +113,13 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
 //  - K operand: used as is; the constant 1152 contributes 1152 * sum_c q'_c to
 //    every score of a query row, which is subtracted once per block in fp32
 //    (the QK accumulator restarts at zero every block).
-//  - V operand: the PV accumulator runs over all blocks, so 1152 is removed
-//    exactly with one packed fp16 subtract, leaving the code.
+//  - V operand: also used as is; the PV accumulator gathers 1152 * sum p on
+//    top of sum p * code, removed once per ring write (ws_scale_v) from the
+//    row sum of p that the softmax keeps anyway.
 __device__ __forceinline__ void u8x4_to_h2x2_biased(uint32_t w, uint32_t& b0, uint32_t& b1) {
   b0 = __byte_perm(w, 0x64646464u, 0x5140);
   b1 = __byte_perm(w, 0x64646464u, 0x5342);
 }
-__device__ __forceinline__ void u8x4_to_h2x2_exact(uint32_t w, uint32_t& b0, uint32_t& b1) {
-  uint32_t lo = __byte_perm(w, 0x64646464u, 0x5140);
-  uint32_t hi = __byte_perm(w, 0x64646464u, 0x5342);
-  const __half2 bias = __float2half2_rn(1152.0f);
-  __half2 hl = __hsub2(*reinterpret_cast<__half2*>(&lo), bias);
-  __half2 hh = __hsub2(*reinterpret_cast<__half2*>(&hi), bias);
-  b0 = *reinterpret_cast<uint32_t*>(&hl);
-  b1 = *reinterpret_cast<uint32_t*>(&hh);
-}
-
 // 2^x with the hardware approximation (relative error about 2^-22).
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -298,10 +289,23 @@ __device__ __forceinline__ void ws_begin(WarpState<D>& w, const void* q, size_t 
 // Multiply what the INT8 codes accumulated by the per-channel V scale.
 template <int D>
 __device__ __forceinline__ void ws_scale_v(WarpState<D>& w, const float* sVu, int t) {
+  // The INT8 V operand entered the products as fp16 1152 + code (two byte
+  // permutes, no subtraction), so the accumulator holds sum p (1152 + code).
+  // l_run is, up to this point, this lane's sum of the same p (rescaled with
+  // the accumulator): the four lanes of a row add up the row's bias.  The
+  // high and low parts of P sit in rows g and g + 8; the bias of both is
+  // removed from row g, whose sum with row g + 8 is the output.
+  float l = w.l_run;
+  l += __shfl_xor_sync(0xffffffffu, l, 1);
+  l += __shfl_xor_sync(0xffffffffu, l, 2);
+  const float bias = 1152.0f * l;
 #pragma unroll
   for (int j = 0; j < D / 8; ++j) {
     const float2 sv = *reinterpret_cast<const float2*>(sVu + j * 8 + 2 * t);
-    w.acc[j][0] *= sv.x; w.acc[j][1] *= sv.y; w.acc[j][2] *= sv.x; w.acc[j][3] *= sv.y;
+    w.acc[j][0] = (w.acc[j][0] - bias) * sv.x;
+    w.acc[j][1] = (w.acc[j][1] - bias) * sv.y;
+    w.acc[j][2] *= sv.x;
+    w.acc[j][3] *= sv.y;
   }
 }
 
@@ -350,7 +354,7 @@ __device__ __forceinline__ void int8_block(WarpState<D>& w, uint32_t kb, uint32_
 #pragma unroll
   for (int j = 0; j < D / 8; ++j) {
     uint32_t b0, b1;
-    u8x4_to_h2x2_exact(comp(vw[j >> 2], j & 3), b0, b1);
+    u8x4_to_h2x2_biased(comp(vw[j >> 2], j & 3), b0, b1);   // 1152 + code: bias removed in ws_scale_v
     mma16816(w.acc[j], pa, b0, b1);
   }
 }

@@ -979,17 +979,22 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
           int8_block<D>(ws, stage + warp * 16 * D, stage + kHalf + warp * 16 * D, blk, n8, G, g, t,
                         lane, nullptr, sc4buf);
         }
-      } else if (warp < nb) {
-        if (!ws.in_ring) {
-          make_q_frag_s<D>(ws.aq, hdr + hl.q, s.qbf16, nullptr, qs, G, g, t);
-          ws.qoffset = 0.f;
-          ws_scale_v<D>(ws, sVh, t);
-          ws.in_ring = true;
+      } else {
+        // a ring stage holds 2 FP16 blocks: warps 0-1 take the even ring
+        // stages, warps 2-3 the odd ones, so both pairs work at once
+        const int jb = warp - 2 * ((i - sch.n8st) & 1);
+        if (jb >= 0 && jb < nb) {
+          if (!ws.in_ring) {
+            make_q_frag_s<D>(ws.aq, hdr + hl.q, s.qbf16, nullptr, qs, G, g, t);
+            ws.qoffset = 0.f;
+            ws_scale_v<D>(ws, sVh, t);
+            ws.in_ring = true;
+          }
+          const int rb = first + jb;
+          tok0 = s.cap + rb * 16;
+          ring_block<D>(ws, stage + jb * 32 * D, stage + kHalf + jb * 32 * D, posh + rb * 16, G, g, t,
+                        lane, nullptr, sc4buf);
         }
-        const int rb = first + warp;
-        tok0 = s.cap + rb * 16;
-        ring_block<D>(ws, stage + warp * 32 * D, stage + kHalf + warp * 32 * D, posh + rb * 16, G, g, t,
-                      lane, nullptr, sc4buf);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty_bar(st.slot));

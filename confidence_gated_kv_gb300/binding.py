@@ -92,6 +92,8 @@ def lib() -> ctypes.CDLL:
             "confkv_profile_read": (ctypes.c_int, [vp] + [ctypes.POINTER(ctypes.c_double)] * 3 +
                                     [ctypes.POINTER(i32)]),
             "confkv_attention_plan": (ctypes.c_int, [vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]),
+            "confkv_set_attention_ctas": (ctypes.c_int, [vp, i32]),
+            "confkv_attention_grid": (ctypes.c_int, [vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]),
             "confkv_graph_reserve": (ctypes.c_int, [vp, i64]),
             "confkv_graph_advance": (ctypes.c_int, [vp, i64]),
             "confkv_graph_release": (ctypes.c_int, [vp]),
@@ -372,3 +374,14 @@ class Cache:
         _check(lib().confkv_attention_plan(self._h, ctypes.byref(sp), ctypes.byref(sm)),
                "confkv_attention_plan")
         return int(sp.value), int(sm.value)
+
+    def set_attention_ctas(self, ctas):
+        """Cap the persistent attention grid at `ctas` CTAs (0: two per SM)."""
+        _check(lib().confkv_set_attention_ctas(self._h, int(ctas)), "confkv_set_attention_ctas")
+
+    def attention_grid(self):
+        """(CTAs, cluster size) of the next attention launch."""
+        g, c = ctypes.c_int32(), ctypes.c_int32()
+        _check(lib().confkv_attention_grid(self._h, ctypes.byref(g), ctypes.byref(c)),
+               "confkv_attention_grid")
+        return int(g.value), int(c.value)

@@ -111,6 +111,7 @@ size_t layout(const Shape& s, char* base, Dev* d, Staging* st) {
   dd.status = cv.take<int32_t>(1);
   dd.absmax = cv.take<uint32_t>(2 * units * s.D);
   dd.score_ctas = attention_persistent_ctas();
+  dd.attn_ctas = 0;
   dd.scores = cv.take<float>((size_t)dd.score_ctas * 2 * s.G * s.S);
   dd.step_dev = cv.take<long long>(1);
   dd.sel_done = cv.take<uint32_t>(1);
@@ -261,8 +262,12 @@ static int plan_attention_for(const confkv_ctx* ctx, long long n8_bound, int* sp
   const long long units = (long long)s.L * s.B * s.Hkv;
   const int nbT = max_tokens / 16;
   int splits = 1;
-  // enough CTAs to fill the GPU a few times over, at least 4 blocks per CTA
-  while (splits < kMaxSplits && units * splits < 4LL * kNumSMs && nbT / (splits * 2) >= 4) splits *= 2;
+  // enough CTAs to fill the GPU a few times over, at least 4 blocks per CTA,
+  // and no more CTAs than the caller's cap on the attention grid
+  const long long cap = ctx->d.attn_ctas;
+  while (splits < kMaxSplits && units * splits < 4LL * kNumSMs && nbT / (splits * 2) >= 4 &&
+         (cap == 0 || units * splits * 2 <= cap))
+    splits *= 2;
   while (splits < kMaxSplits && attention_smem_bytes(s, splits, max_tokens) > attention_max_smem())
     splits *= 2;
   if (attention_smem_bytes(s, splits, max_tokens) > attention_max_smem()) return CONFKV_ECAPACITY;
@@ -308,6 +313,24 @@ int confkv_attention_plan(confkv_ctx* ctx, int32_t* splits, int32_t* smem_bytes)
   if (r != CONFKV_OK) return r;
   *splits = sp;
   *smem_bytes = attention_smem_bytes(ctx->s, sp, mt);
+  return CONFKV_OK;
+}
+
+int confkv_set_attention_ctas(confkv_ctx* ctx, int32_t ctas) {
+  if (!ctx || ctas < 0) return CONFKV_EINVAL;
+  ctx->d.attn_ctas = ctas;
+  return CONFKV_OK;
+}
+
+int confkv_attention_grid(confkv_ctx* ctx, int32_t* ctas, int32_t* cluster) {
+  if (!ctx || !ctas || !cluster) return CONFKV_EINVAL;
+  int sp = 0, mt = 0;
+  const int r = plan_attention(ctx, &sp, &mt);
+  if (r != CONFKV_OK) return r;
+  int g = 0, c = 0;
+  attention_grid(ctx->s, ctx->d, sp, &g, &c);
+  *ctas = g;
+  *cluster = c;
   return CONFKV_OK;
 }
 

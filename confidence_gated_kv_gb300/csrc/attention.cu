@@ -210,10 +210,12 @@ __device__ __forceinline__ void softmax_block(float (&sc4)[2][2], const bool (&v
       if (!valid[nt][j] || g >= G) sc4[nt][j] = -INFINITY;
       mloc = fmaxf(mloc, sc4[nt][j]);
     }
-  mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
-  mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
-  const bool move = mloc > m_run + 8.0f;     // true for the first finite block too
-  if (__any_sync(0xffffffffu, move)) {
+  // The row maximum of the four lanes exceeds m_run + 8 exactly when one
+  // lane's own maximum does, so the quad reduction runs only then.
+  if (__any_sync(0xffffffffu, mloc > m_run + 8.0f)) {
+    mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 1));
+    mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 2));
+    const bool move = mloc > m_run + 8.0f;   // true for the first finite block too
     const float corr = move ? (m_run == -INFINITY ? 0.f : ex2(m_run - mloc)) : 1.0f;
     if (move) m_run = mloc;
     l_run *= corr;
@@ -1096,6 +1098,20 @@ static int num_sms() {
 
 int attention_persistent_ctas() { return 2 * num_sms(); }
 
+void attention_grid(const Shape& s, const Dev& d, int splits, int* grid_out, int* cluster_out) {
+  const int units = s.L * s.B * s.Hkv;
+  if (splits > 1) {
+    *grid_out = units * splits;
+    *cluster_out = splits;
+    return;
+  }
+  int grid = units < 2 * num_sms() ? units : 2 * num_sms();
+  if (grid > d.score_ctas) grid = d.score_ctas;
+  if (d.attn_ctas > 0 && grid > d.attn_ctas) grid = d.attn_ctas;
+  *grid_out = grid;
+  *cluster_out = 1;
+}
+
 // Self-test of the bounded-wait path: one CTA waits on an mbarrier that no
 // thread ever arrives on, with a short poll limit, then reports the time-out
 // through the device status word exactly as the decode kernels do.  Nothing
@@ -1137,8 +1153,8 @@ static int launch_d(const Shape& s, const Dev& d, const void* q, float* out, int
         return -1;
       configured = true;
     }
-    int grid = units < 2 * num_sms() ? units : 2 * num_sms();
-    if (grid > d.score_ctas) grid = d.score_ctas;
+    int grid = 0, cluster = 0;
+    attention_grid(s, d, 1, &grid, &cluster);
     return launch_pdl(attention_persistent_kernel<D>, dim3(grid), dim3(kPThreads), (size_t)smem, stream,
                       s, d, q, out, budget, conf_out, stages_persistent(s)) == cudaSuccess
                ? 0

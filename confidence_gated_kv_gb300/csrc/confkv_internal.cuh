@@ -128,6 +128,7 @@ struct Dev {
   uint32_t* absmax;                // [2][l][b][kvh][D] prefill scratch
   float* scores;                   // [persistent CTAs][2][G][S] attention score scratch
   int score_ctas;                  // persistent attention CTAs the score scratch holds
+  int attn_ctas;                   // cap on the persistent attention grid (0 = none)
   long long* step_dev;             // decode steps done since prefill (read by prestep and select)
   uint32_t* sel_done;              // select CTAs finished in the current step (0 between steps)
 };
@@ -191,6 +192,9 @@ int launch_prestep(const Shape& s, const Dev& d, long long step, const float* lo
                    const void* k_new, const void* v_new, cudaStream_t stream);
 int launch_attention(const Shape& s, const Dev& d, const void* q, float* out, int32_t* budget,
                      float* conf_out, int splits, int max_tokens, cudaStream_t stream);
+// Grid and cluster size of the attention launch for `splits` CTAs per unit
+// (the persistent kernel when 1, whose CTAs are not clustered).
+void attention_grid(const Shape& s, const Dev& d, int splits, int* grid, int* cluster);
 int launch_select(const Shape& s, const Dev& d, long long step, int32_t* evicted_pos,
                   int32_t* n_evicted, cudaStream_t stream);
 int attention_smem_bytes(const Shape& s, int splits, int max_tokens);

@@ -278,6 +278,25 @@ int confkv_profile_read(confkv_ctx* ctx, double* ms_prestep, double* ms_attentio
  * KV head) and dynamic shared memory per CTA. */
 int confkv_attention_plan(confkv_ctx* ctx, int32_t* splits, int32_t* smem_bytes);
 
+/* Caps the attention grid at `ctas` CTAs; 0 (the default) lets the
+ * persistent kernel use two CTAs per SM.  The split-K kernel is chosen only
+ * while units x splits stays within the cap, otherwise the persistent kernel
+ * runs on at most `ctas` CTAs.  A smaller grid leaves SMs to work on other
+ * streams, at a proportional cost in attention time.  Takes effect at the
+ * next launch (a captured graph keeps the grid it was captured with; steps
+ * inside a graph reservation keep the reserved plan).  Results do not depend
+ * on it.  The pages give no counterpart: it is a
+ * launch-shape control of this library.  CONFKV_EINVAL for a null ctx or a
+ * negative count. */
+int confkv_set_attention_ctas(confkv_ctx* ctx, int32_t ctas);
+
+/* Grid of the attention launch chosen for the next step: `ctas` CTAs in
+ * clusters of `cluster`.  The persistent kernel (one CTA per unit in
+ * confkv_attention_plan) runs unclustered CTAs that each walk whole
+ * (layer, sequence, KV head) units; the split-K kernel runs one cluster of
+ * `splits` CTAs per unit. */
+int confkv_attention_grid(confkv_ctx* ctx, int32_t* ctas, int32_t* cluster);
+
 /* Byte offset of (token tau in [0,16), channel c) inside one 16-token block of
  * the device layout: kind 0 = INT8 K, 1 = INT8 V, 2 = FP16 K, 3 = FP16 V.
  * Host-only helper for tests of the interleave; -1 for bad arguments. */

@@ -118,6 +118,8 @@ def test_null_handles_are_rejected():
     assert L.confkv_step(None, *([None] * 9), None) == binding.EINVAL
     assert L.confkv_prefill(None, None, None, None, 0, None) == binding.EINVAL
     assert L.confkv_get_stats(None, None, None) == binding.EINVAL
+    assert L.confkv_set_attention_ctas(None, 0) == binding.EINVAL
+    assert L.confkv_attention_grid(None, None, None) == binding.EINVAL
     L.confkv_destroy(None)
 
 

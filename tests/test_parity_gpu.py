@@ -49,6 +49,37 @@ def test_gqa8_pyramidal_budgets():
     assert p.flags.evictions > 0
 
 
+def test_persistent_kernel_several_units_per_cta_under_a_cta_cap():
+    # 12 units (3 sequences x 2 layers x 2 KV heads).  A cap of 5 CTAs runs
+    # the persistent kernel with 2 or 3 units per CTA (the double-buffered
+    # header, partials and score slots turn over; rounds end ragged), a cap of
+    # 4 with 3 units on every CTA.  Without a cap so few units take the
+    # split-K cluster kernel.  The empty prefill gives one sequence units of
+    # ring blocks only.
+    w = Workload(name="t_cap", B=3, L=2, Hq=10, Hkv=2, d=128, V=3000, T0=300, steps=36,
+                 n_high=(40, 30), n_low=(120, 90), P=8, W=32, q_dtype="bf16",
+                 heavy_count=5, heavy_factor=3.0, logit_sigma=1.5, spike_hi=14.0)
+    p = Pair(w, 31, prefill_len=[300, 17, 0])
+    s = 0
+    for cap, grid in [(5, (5, 1)), (4, (4, 1)), (0, None)]:
+        p.cache.set_attention_ctas(cap)
+        splits = p.cache.attention_plan()[0]
+        if grid is None:
+            assert splits > 1
+            grid = (12 * splits, splits)
+        else:
+            assert splits == 1
+        assert p.cache.attention_grid() == grid
+        for _ in range(12):
+            q, kn, vn, lg = step_inputs(w, 31, s)
+            if s % 5 == 4:
+                lg = confident_logits(w.V, w.B, 31000 + s)
+            p.step(q, kn, vn, lg)
+            s += 1
+    assert p.flags.evictions > 0
+    assert p.flags.max_out_err <= 2e-3
+
+
 def test_split_k_cluster_path_and_large_first_eviction():
     w = Workload(name="t_split", B=1, L=1, Hq=8, Hkv=2, d=128, V=4000, T0=2000, steps=6,
                  n_high=(300,), n_low=(600,), P=16, W=64, q_dtype="bf16", heavy_count=10,

@@ -328,8 +328,8 @@ def run_ours(args):
             cache.step_host(hq[j], hk[j], hv[j], hl[j], hout)
         e_el = time.perf_counter() - e0
         hst = cache.stats()
-        # the library reports the bytes it copied (evicted rows only up to the
-        # step's worst-case eviction count)
+        # pinned buffers: the library's mapped mode (kernels read and write the
+        # host buffers in place, q staged); it reports the bytes that crossed
         h2d, d2h = hst["host_h2d_bytes"] or h2d, hst["host_d2h_bytes"] or d2h
         e2e = {"value": ws * args.e2e_steps / e_el, "unit": "steps/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),

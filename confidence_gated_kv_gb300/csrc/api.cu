@@ -151,7 +151,7 @@ struct confkv_ctx {
   // confkv_step_host: a second stream copies the attention output back while
   // the select kernel runs (created on first use)
   cudaStream_t aux = nullptr;
-  cudaEvent_t ev_attn = nullptr, ev_aux = nullptr;
+  cudaEvent_t ev_attn = nullptr, ev_aux = nullptr, ev_in = nullptr, ev_q = nullptr;
   // profiling
   bool prof_on = false;
   int prof_max = 0, prof_count = 0;
@@ -219,6 +219,8 @@ void confkv_destroy(confkv_ctx* ctx) {
   for (cudaEvent_t e : ctx->ev) cudaEventDestroy(e);
   if (ctx->ev_attn) cudaEventDestroy(ctx->ev_attn);
   if (ctx->ev_aux) cudaEventDestroy(ctx->ev_aux);
+  if (ctx->ev_in) cudaEventDestroy(ctx->ev_in);
+  if (ctx->ev_q) cudaEventDestroy(ctx->ev_q);
   if (ctx->aux) cudaStreamDestroy(ctx->aux);
   delete ctx;
 }
@@ -336,7 +338,8 @@ int confkv_attention_grid(confkv_ctx* ctx, int32_t* ctas, int32_t* cluster) {
 
 static int step_impl(confkv_ctx* ctx, const void* q, const void* k_new, const void* v_new,
                      const float* logits, float* out, int32_t* budget, float* confidence,
-                     int32_t* evicted_pos, int32_t* n_evicted, void* stream, cudaEvent_t after_attention);
+                     int32_t* evicted_pos, int32_t* n_evicted, void* stream, cudaEvent_t after_attention,
+                     cudaEvent_t before_attention = nullptr);
 
 int confkv_step(confkv_ctx* ctx, const void* q, const void* k_new, const void* v_new,
                 const float* logits, float* out, int32_t* budget, float* confidence,
@@ -346,10 +349,12 @@ int confkv_step(confkv_ctx* ctx, const void* q, const void* k_new, const void* v
 }
 
 // after_attention: recorded on `stream` once the attention kernel (the last
-// writer of `out`) has been launched, when not null
+// writer of `out`) has been launched, when not null; before_attention: waited
+// for on `stream` before the attention kernel is launched, when not null
 static int step_impl(confkv_ctx* ctx, const void* q, const void* k_new, const void* v_new,
                      const float* logits, float* out, int32_t* budget, float* confidence,
-                     int32_t* evicted_pos, int32_t* n_evicted, void* stream, cudaEvent_t after_attention) {
+                     int32_t* evicted_pos, int32_t* n_evicted, void* stream, cudaEvent_t after_attention,
+                     cudaEvent_t before_attention) {
   if (!ctx) return CONFKV_EINVAL;
   if (!ctx->prefilled) return CONFKV_ESTATE;
   if (!q || !k_new || !v_new || !logits || !out || !budget || !evicted_pos || !n_evicted)
@@ -379,6 +384,7 @@ static int step_impl(confkv_ctx* ctx, const void* q, const void* k_new, const vo
   const long long step_arg = (capturing || ctx->pin_left > 0) ? -1 : ctx->steps;
   if (launch_prestep(s, ctx->d, step_arg, logits, k_new, v_new, st) != 0) return CONFKV_ECUDA;
   if (prof) cudaEventRecord(ev[1], st);
+  if (before_attention && cudaStreamWaitEvent(st, before_attention, 0) != cudaSuccess) return CONFKV_ECUDA;
   if (launch_attention(s, ctx->d, q, out, budget, confidence, splits, max_tokens, st) != 0)
     return CONFKV_ECUDA;
   if (prof) cudaEventRecord(ev[2], st);
@@ -448,6 +454,20 @@ int confkv_graph_release(confkv_ctx* ctx) {
   return CONFKV_OK;
 }
 
+// Device address of page-locked host memory, if `p` lies in such memory (an
+// allocation of cudaHostAlloc / cudaMallocHost or a cudaHostRegister range)
+// and the device can address it; false for pageable or device memory.
+static bool device_view(const void* p, void** dev) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr) return false;
+  *dev = a.devicePointer;
+  return true;
+}
+
 int confkv_step_host(confkv_ctx* ctx, const void* q, const void* k_new, const void* v_new,
                      const float* logits, float* out, int32_t* budget, float* confidence,
                      int32_t* evicted_pos, int32_t* n_evicted, void* stream) {
@@ -462,6 +482,44 @@ int confkv_step_host(confkv_ctx* ctx, const void* q, const void* k_new, const vo
   if (cs != cudaStreamCaptureStatusNone) return CONFKV_ESTATE;   // host copies stay outside graphs
   const size_t lbs = (size_t)s.L * s.B;
   const size_t nq = lbs * s.Hq * s.D * 2, nkv = lbs * s.Hkv * s.D * 2;
+  if (!ctx->aux) {
+    if (cudaStreamCreateWithFlags(&ctx->aux, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ctx->ev_attn, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ctx->ev_aux, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ctx->ev_in, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ctx->ev_q, cudaEventDisableTiming) != cudaSuccess)
+      return CONFKV_ECUDA;
+  }
+  // Mapped mode: when every buffer but q is page-locked host memory that the
+  // device can address, the kernels read logits and the new K/V and write
+  // every output in place over the host link, and only q (read by the bulk
+  // copies of the attention kernel) is staged, on the second stream while
+  // the first kernel runs.
+  void *mk = nullptr, *mv = nullptr, *ml = nullptr, *mo = nullptr, *mb = nullptr, *mc = nullptr,
+       *me = nullptr, *mn = nullptr;
+  const bool mapped = device_view(k_new, &mk) && device_view(v_new, &mv) && device_view(logits, &ml) &&
+                      device_view(out, &mo) && device_view(budget, &mb) &&
+                      (!confidence || device_view(confidence, &mc)) && device_view(evicted_pos, &me) &&
+                      device_view(n_evicted, &mn);
+  if (mapped) {
+    cudaError_t e = cudaEventRecord(ctx->ev_in, st);   // g.q is free once earlier work on `stream` is
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->aux, ctx->ev_in, 0);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(g.q, q, nq, cudaMemcpyHostToDevice, ctx->aux);
+    if (e == cudaSuccess) e = cudaEventRecord(ctx->ev_q, ctx->aux);
+    if (e != cudaSuccess) return CONFKV_ECUDA;
+    const int r = step_impl(ctx, g.q, mk, mv, static_cast<const float*>(ml), static_cast<float*>(mo),
+                            static_cast<int32_t*>(mb), confidence ? static_cast<float*>(mc) : nullptr,
+                            static_cast<int32_t*>(me), static_cast<int32_t*>(mn), stream, nullptr, ctx->ev_q);
+    if (r != CONFKV_OK) return r;
+    e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_status(e);
+    long long written = 0;
+    for (size_t i = 0; i < lbs; ++i) written += n_evicted[i] > 0 ? n_evicted[i] : 0;
+    ctx->host_h2d = (long long)(nq + 2 * nkv + (size_t)s.B * s.V * 4);
+    ctx->host_d2h = (long long)(lbs * s.Hq * s.D * 4 + lbs * 4 + (confidence ? (size_t)s.B * 4 : 0) +
+                                (size_t)written * 4 + lbs * 4);
+    return CONFKV_OK;
+  }
   cudaError_t e = cudaMemcpyAsync(g.q, q, nq, cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(g.k_new, k_new, nkv, cudaMemcpyHostToDevice, st);
   if (e == cudaSuccess) e = cudaMemcpyAsync(g.v_new, v_new, nkv, cudaMemcpyHostToDevice, st);
@@ -471,12 +529,6 @@ int confkv_step_host(confkv_ctx* ctx, const void* q, const void* k_new, const vo
   // no row of evicted positions can hold more than this step's eviction bound
   const long long k_bound =
       std::min<long long>(s.max_evict, std::max(0LL, ctx->n_bound - ctx->minN));
-  if (!ctx->aux) {
-    if (cudaStreamCreateWithFlags(&ctx->aux, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaEventCreateWithFlags(&ctx->ev_attn, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&ctx->ev_aux, cudaEventDisableTiming) != cudaSuccess)
-      return CONFKV_ECUDA;
-  }
   const int r = step_impl(ctx, g.q, g.k_new, g.v_new, g.logits, g.out, g.budget,
                           confidence ? g.conf : nullptr, g.evicted, g.nevict, stream, ctx->ev_attn);
   if (r != CONFKV_OK) return r;

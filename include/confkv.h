@@ -152,15 +152,22 @@ int confkv_step(confkv_ctx* ctx, const void* q, const void* k_new, const void* v
                 int32_t* evicted_pos, int32_t* n_evicted, void* stream);
 
 /*
- * confkv_step with HOST buffers (same shapes): copies the inputs to device
- * staging buffers inside the workspace, runs the step and copies the outputs
- * back, then synchronises.  The attention output is copied back on a second,
- * library-owned stream (created on the first call) while the last kernel of
- * the step runs; everything else runs on `stream`, and the call returns
- * after both are done.  Pinned host memory makes the copies asynchronous
- * DMA.  confidence may be NULL.  Of each row
- * of evicted_pos only the entries the step could write are copied back (as
- * many as its worst-case eviction count); the rest of the row is untouched.
+ * confkv_step with HOST buffers (same shapes); returns once the outputs are
+ * in the host buffers.  Two modes, chosen per call, with identical results:
+ *  - mapped: when k_new, v_new, logits and every output buffer lie in
+ *    page-locked host memory the device can address (cudaHostAlloc,
+ *    cudaMallocHost or cudaHostRegister), the kernels read those inputs and
+ *    write those outputs in place over the host link.  Only q is copied, to
+ *    a staging buffer inside the workspace, on a second library-owned
+ *    stream (created on the first call) while the first kernel runs.
+ *  - staged: otherwise every input is copied to staging buffers inside the
+ *    workspace first, and the outputs are copied back (the attention output
+ *    on the second stream while the last kernel runs).  Pinned memory makes
+ *    these copies asynchronous DMA.
+ * confidence may be NULL.  Of each row of evicted_pos only the first
+ * n_evicted entries are meaningful; in mapped mode only those are written,
+ * in staged mode as many as the step's worst-case eviction count are copied
+ * back.  The rest of the row is untouched.
  */
 int confkv_step_host(confkv_ctx* ctx, const void* q, const void* k_new, const void* v_new,
                      const float* logits, float* out, int32_t* budget, float* confidence,
@@ -252,8 +259,8 @@ typedef struct confkv_stats {
   int64_t resident;          /* cache entries resident now, all units */
   int64_t resident_bytes;    /* K/V bytes resident now at stored widths */
   int32_t device_status;     /* raw device status bits (0 = ok) */
-  int64_t host_h2d_bytes;    /* bytes the last confkv_step_host copied to the device */
-  int64_t host_d2h_bytes;    /* bytes the last confkv_step_host copied back */
+  int64_t host_h2d_bytes;    /* bytes the last confkv_step_host moved host -> device */
+  int64_t host_d2h_bytes;    /* bytes the last confkv_step_host moved device -> host */
 } confkv_stats;
 
 /* Read the counters and the device status word (synchronises `stream`).

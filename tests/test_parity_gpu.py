@@ -240,7 +240,10 @@ def test_gpt2_small_batch8_pyramid_prefix():
     p.compare_states()
 
 
-def test_host_buffer_step_matches_device_step():
+@pytest.mark.parametrize("pinned", [True, False, "mixed"])
+def test_host_buffer_step_matches_device_step(pinned):
+    # pinned buffers take the mapped mode (kernels read and write host memory
+    # in place); pageable ones, or a mix, the staged copies
     w = Workload(name="t_host", B=2, L=2, Hq=8, Hkv=2, d=128, V=3000, T0=100, steps=5,
                  n_high=(40, 40), n_low=(64, 64), P=8, W=16, q_dtype="bf16")
     k, v = prefill_batch(w, 16, "cpu")
@@ -248,12 +251,15 @@ def test_host_buffer_step_matches_device_step():
     b = ck.Cache(ck.config_from_workload(w))
     a.prefill(k.cuda(), v.cuda(), [w.T0] * w.B)
     b.prefill(k.cuda(), v.cuda(), [w.T0] * w.B)
-    hout = b.host_outputs()
+    hout = b.host_outputs(pin=pinned is not False)
+    pin_in = pinned is True
     for s in range(5):
         q, kn, vn, lg = step_inputs(w, 16, s)
         o = a.step(q.cuda(), kn.cuda(), vn.cuda(), lg.cuda())
-        b.step_host(q.pin_memory(), kn.pin_memory(), vn.pin_memory(), lg.pin_memory(), hout)
+        ins = [x.pin_memory() if pin_in else x.clone() for x in (q, kn, vn, lg)]
+        b.step_host(*ins, hout)
         torch.cuda.synchronize()
+        assert b.stats()["host_h2d_bytes"] == sum(x.numel() * x.element_size() for x in (q, kn, vn, lg))
         assert torch.equal(o["out"].cpu(), hout["out"])
         assert torch.equal(o["budget"].cpu(), hout["budget"])
         assert torch.equal(o["n_evicted"].cpu(), hout["n_evicted"])

@@ -106,6 +106,7 @@ size_t layout(const Shape& s, char* base, Dev* d, Staging* st) {
   dd.n_low = cv.take<int32_t>(s.L);
   dd.conf = cv.take<ConfPartial>((size_t)s.B * s.SV);
   dd.cval = cv.take<double>(s.B);
+  dd.conf_done = cv.take<uint32_t>(s.B);
   dd.scratch = cv.take<uint32_t>(lbs * s.S);
   dd.stats = cv.take<DevStats>(1);
   dd.status = cv.take<int32_t>(1);
@@ -205,6 +206,7 @@ int confkv_create(const confkv_config* cfg, void* workspace, size_t workspace_by
   if (e == cudaSuccess) e = cudaMemset(c->d.status, 0, sizeof(int32_t));
   if (e == cudaSuccess) e = cudaMemset(c->d.step_dev, 0, sizeof(long long));
   if (e == cudaSuccess) e = cudaMemset(c->d.sel_done, 0, sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaMemset(c->d.conf_done, 0, s.B * sizeof(uint32_t));
   if (e != cudaSuccess) {
     delete c;
     return CONFKV_ECUDA;
@@ -244,6 +246,7 @@ int confkv_prefill(confkv_ctx* ctx, const int32_t* prefill_len, const void* k, c
   if (e == cudaSuccess) e = cudaMemsetAsync(ctx->d.status, 0, sizeof(int32_t), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(ctx->d.step_dev, 0, sizeof(long long), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(ctx->d.sel_done, 0, sizeof(uint32_t), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ctx->d.conf_done, 0, s.B * sizeof(uint32_t), st);
   if (e != cudaSuccess) return CONFKV_ECUDA;
   if (launch_prefill(s, ctx->d, k, v, t_max, ctx->T0.data(), st) != 0) return CONFKV_ECUDA;
   // the host copy of T0 is pageable: make sure it has been consumed
@@ -339,7 +342,7 @@ int confkv_attention_grid(confkv_ctx* ctx, int32_t* ctas, int32_t* cluster) {
 static int step_impl(confkv_ctx* ctx, const void* q, const void* k_new, const void* v_new,
                      const float* logits, float* out, int32_t* budget, float* confidence,
                      int32_t* evicted_pos, int32_t* n_evicted, void* stream, cudaEvent_t after_attention,
-                     cudaEvent_t before_attention = nullptr);
+                     cudaEvent_t before_attention = nullptr, bool conf_in_attention = false);
 
 int confkv_step(confkv_ctx* ctx, const void* q, const void* k_new, const void* v_new,
                 const float* logits, float* out, int32_t* budget, float* confidence,
@@ -350,11 +353,14 @@ int confkv_step(confkv_ctx* ctx, const void* q, const void* k_new, const void* v
 
 // after_attention: recorded on `stream` once the attention kernel (the last
 // writer of `out`) has been launched, when not null; before_attention: waited
-// for on `stream` before the attention kernel is launched, when not null
+// for on `stream` before the attention kernel is launched, when not null;
+// conf_in_attention: reduce the logits to confidence partials in the
+// persistent attention kernel rather than in the prestep kernel (logits in
+// host memory: their transfer then overlaps the attention).
 static int step_impl(confkv_ctx* ctx, const void* q, const void* k_new, const void* v_new,
                      const float* logits, float* out, int32_t* budget, float* confidence,
                      int32_t* evicted_pos, int32_t* n_evicted, void* stream, cudaEvent_t after_attention,
-                     cudaEvent_t before_attention) {
+                     cudaEvent_t before_attention, bool conf_in_attention) {
   if (!ctx) return CONFKV_EINVAL;
   if (!ctx->prefilled) return CONFKV_ESTATE;
   if (!q || !k_new || !v_new || !logits || !out || !budget || !evicted_pos || !n_evicted)
@@ -382,10 +388,12 @@ static int step_impl(confkv_ctx* ctx, const void* q, const void* k_new, const vo
   // inside a graph reservation every step (captured or not) takes its index
   // from the device counter, which the reservation set and each step advances
   const long long step_arg = (capturing || ctx->pin_left > 0) ? -1 : ctx->steps;
-  if (launch_prestep(s, ctx->d, step_arg, logits, k_new, v_new, st) != 0) return CONFKV_ECUDA;
+  const bool attn_conf = conf_in_attention && splits == 1;
+  if (launch_prestep(s, ctx->d, step_arg, logits, k_new, v_new, !attn_conf, st) != 0) return CONFKV_ECUDA;
   if (prof) cudaEventRecord(ev[1], st);
   if (before_attention && cudaStreamWaitEvent(st, before_attention, 0) != cudaSuccess) return CONFKV_ECUDA;
-  if (launch_attention(s, ctx->d, q, out, budget, confidence, splits, max_tokens, st) != 0)
+  if (launch_attention(s, ctx->d, q, out, budget, confidence, attn_conf ? logits : nullptr, splits,
+                       max_tokens, st) != 0)
     return CONFKV_ECUDA;
   if (prof) cudaEventRecord(ev[2], st);
   if (after_attention && cudaEventRecord(after_attention, st) != cudaSuccess) return CONFKV_ECUDA;
@@ -509,7 +517,8 @@ int confkv_step_host(confkv_ctx* ctx, const void* q, const void* k_new, const vo
     if (e != cudaSuccess) return CONFKV_ECUDA;
     const int r = step_impl(ctx, g.q, mk, mv, static_cast<const float*>(ml), static_cast<float*>(mo),
                             static_cast<int32_t*>(mb), confidence ? static_cast<float*>(mc) : nullptr,
-                            static_cast<int32_t*>(me), static_cast<int32_t*>(mn), stream, nullptr, ctx->ev_q);
+                            static_cast<int32_t*>(me), static_cast<int32_t*>(mn), stream, nullptr, ctx->ev_q,
+                            true);
     if (r != CONFKV_OK) return r;
     e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_status(e);

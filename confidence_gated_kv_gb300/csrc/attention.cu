@@ -738,7 +738,8 @@ struct RingPos {
 template <int D>
 __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
     Shape s, Dev d, const void* __restrict__ q, float* __restrict__ out,
-    int32_t* __restrict__ budget, float* __restrict__ conf_out, int stages) {
+    int32_t* __restrict__ budget, float* __restrict__ conf_out, const float* __restrict__ logits,
+    int stages) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   constexpr int kStageBytes = 128 * D;
   constexpr int kHalf = kStageBytes / 2;
@@ -850,9 +851,30 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
 
   if (warp == kPConsumers + 1) {
     // ------------------------------------------------ epilogue warp
-    // Idle until the first unit is done: merge the confidence of the
-    // sequences this CTA owns (the prestep kernel wrote their partials).
-    for (int b = blockIdx.x; b < s.B; b += gridDim.x) conf_merge_warp(s, d, b, budget, conf_out);
+    // Idle until the first unit is done: the confidence of the step.
+    if (logits) {
+      // Logits in host memory: this CTA reduces its vocabulary chunks to
+      // partials here, so that their transfer overlaps the attention; the
+      // CTA that finishes the last chunk of a sequence merges that sequence.
+      for (int c = blockIdx.x; c < s.B * s.SV; c += gridDim.x) {
+        const int b = c / s.SV;
+        conf_partial_warp(s, d, logits, b, c % s.SV);
+        unsigned int prev = 0;
+        if (lane == 0) {
+          __threadfence();
+          prev = atomicAdd(d.conf_done + b, 1u);
+        }
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev == (unsigned int)s.SV - 1u) {
+          __threadfence();
+          conf_merge_warp(s, d, b, budget, conf_out);
+          if (lane == 0) d.conf_done[b] = 0u;   // zero again for the next launch
+        }
+      }
+    } else {
+      // the prestep kernel wrote the partials: merge the sequences this CTA owns
+      for (int b = blockIdx.x; b < s.B; b += gridDim.x) conf_merge_warp(s, d, b, budget, conf_out);
+    }
     int k = 0;
     for (int u = blockIdx.x; u < units; u += gridDim.x, ++k) {
       const int ps = k & 1;
@@ -1139,7 +1161,8 @@ int launch_selftest_timeout(const Dev& d, cudaStream_t stream) {
 
 template <int D>
 static int launch_d(const Shape& s, const Dev& d, const void* q, float* out, int32_t* budget,
-                    float* conf_out, int splits, int max_tokens, cudaStream_t stream) {
+                    float* conf_out, const float* logits, int splits, int max_tokens,
+                    cudaStream_t stream) {
   const int chunk = chunk_of(splits, max_tokens);
   const int smem = attention_smem_bytes(s, splits, max_tokens);
   if (smem > attention_max_smem()) return -1;
@@ -1156,7 +1179,7 @@ static int launch_d(const Shape& s, const Dev& d, const void* q, float* out, int
     int grid = 0, cluster = 0;
     attention_grid(s, d, 1, &grid, &cluster);
     return launch_pdl(attention_persistent_kernel<D>, dim3(grid), dim3(kPThreads), (size_t)smem, stream,
-                      s, d, q, out, budget, conf_out, stages_persistent(s)) == cudaSuccess
+                      s, d, q, out, budget, conf_out, logits, stages_persistent(s)) == cudaSuccess
                ? 0
                : -1;
   }
@@ -1185,9 +1208,11 @@ static int launch_d(const Shape& s, const Dev& d, const void* q, float* out, int
 }
 
 int launch_attention(const Shape& s, const Dev& d, const void* q, float* out, int32_t* budget,
-                     float* conf_out, int splits, int max_tokens, cudaStream_t stream) {
-  if (s.D == 128) return launch_d<128>(s, d, q, out, budget, conf_out, splits, max_tokens, stream);
-  if (s.D == 64) return launch_d<64>(s, d, q, out, budget, conf_out, splits, max_tokens, stream);
+                     float* conf_out, const float* logits, int splits, int max_tokens,
+                     cudaStream_t stream) {
+  if (splits > 1 && logits) return -1;   // the split-K kernel merges partials of the prestep kernel
+  if (s.D == 128) return launch_d<128>(s, d, q, out, budget, conf_out, logits, splits, max_tokens, stream);
+  if (s.D == 64) return launch_d<64>(s, d, q, out, budget, conf_out, logits, splits, max_tokens, stream);
   return -1;
 }
 

@@ -58,20 +58,115 @@ __device__ __forceinline__ FSum fsum_shfl_xor(FSum a, int o) {
   return FSum{__shfl_xor_sync(0xffffffffu, a.hi, o), __shfl_xor_sync(0xffffffffu, a.lo, o)};
 }
 
-// Called by all 32 lanes of one warp; publishes c (d.cval, conf_out) and the
-// budget of every layer of sequence b.
-__device__ __forceinline__ void conf_merge_warp(const Shape& s, const Dev& d, int b,
-                                                int32_t* budget, float* conf_out) {
+// (S, T) of a running maximum m_old carried over to a larger one m_new:
+// S <- S e^(m_old - m_new), T <- e^(m_old - m_new) (T + (m_old - m_new) S).
+__device__ __forceinline__ void conf_rescale(FSum& S, FSum& T, float m_old, float m_new) {
+  if (m_old == -FLT_MAX) return;   // nothing summed yet (S = T = 0)
+  const float dm = m_old - m_new;
+  const float f = expf(dm);
+  T = fsum_add(T, dm * S.hi);
+  T = fsum_add(T, dm * S.lo);
+  T = FSum{T.hi * f, T.lo * f};
+  S = FSum{S.hi * f, S.lo * f};
+}
+
+// Partial (M, S, T, top 2) of vocabulary chunk `part` of sequence b, computed
+// by one warp in a single pass over the logits: each lane keeps its own
+// running maximum and carries its sums over when it moves, then the lanes are
+// brought to the chunk maximum and summed.  Called by all 32 lanes.
+__device__ __forceinline__ void conf_partial_warp(const Shape& s, const Dev& d,
+                                                  const float* __restrict__ logits, int b, int part) {
+  constexpr int kIn = 8;   // loads in flight per lane
   const int lane = threadIdx.x & 31;
-  const ConfPartial* cp = d.conf + (size_t)b * s.SV;
+  const int V = s.V;
+  const int chunk = (V + s.SV - 1) / s.SV;
+  const int v0 = part * chunk, v1 = min(V, v0 + chunk);
+  const float* z = logits + (size_t)b * V;
+  float m = -FLT_MAX;
+  FSum S{0.f, 0.f}, T{0.f, 0.f};
+  Top2 tp{-FLT_MAX, -FLT_MAX, 0x7fffffff};
+  for (int base = v0; base < v1; base += 32 * kIn) {
+    float x[kIn];
+#pragma unroll
+    for (int j = 0; j < kIn; ++j) {
+      const int idx = base + 32 * j + lane;
+      x[j] = idx < v1 ? __ldg(z + idx) : -FLT_MAX;
+    }
+#pragma unroll
+    for (int j = 0; j < kIn; ++j) {
+      const int idx = base + 32 * j + lane;
+      if (idx < v1) {
+        if (x[j] > m) {
+          conf_rescale(S, T, m, x[j]);
+          m = x[j];
+        }
+        const float dz = x[j] - m;
+        const float e = expf(dz);
+        S = fsum_add(S, e);
+        T = fsum_add(T, dz * e);
+        tp = top2_merge(tp, Top2{x[j], -FLT_MAX, idx});
+      }
+    }
+  }
+  float M = m;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  conf_rescale(S, T, m, M);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    S = fsum_add(S, fsum_shfl_xor(S, o));
+    T = fsum_add(T, fsum_shfl_xor(T, o));
+    Top2 other{__shfl_xor_sync(0xffffffffu, tp.z1, o), __shfl_xor_sync(0xffffffffu, tp.z2, o),
+               __shfl_xor_sync(0xffffffffu, tp.i1, o)};
+    tp = top2_merge(tp, other);
+  }
+  if (lane == 0) {
+    ConfPartial cp;
+    cp.M = (v1 > v0) ? M : -FLT_MAX;
+    cp.z1 = tp.z1;
+    cp.z2 = tp.z2;
+    cp.i1 = tp.i1;
+    cp.S = S.hi;
+    cp.Se = S.lo;
+    cp.T = T.hi;
+    cp.Te = T.lo;
+    d.conf[(size_t)b * s.SV + part] = cp;
+  }
+}
+
+static_assert(sizeof(ConfPartial) == 32, "ConfPartial is read as two 16-byte words");
+
+// One chunk partial read from L2 (written by other CTAs of the same kernel
+// in the attention-side reduction).
+__device__ __forceinline__ ConfPartial load_partial(const ConfPartial* p) {
+  const float4 a = __ldcg(reinterpret_cast<const float4*>(p));
+  const float4 c = __ldcg(reinterpret_cast<const float4*>(p) + 1);
+  ConfPartial r;
+  r.M = a.x;
+  r.z1 = a.y;
+  r.z2 = a.z;
+  r.i1 = __float_as_int(a.w);
+  r.S = c.x;
+  r.Se = c.y;
+  r.T = c.z;
+  r.Te = c.w;
+  return r;
+}
+
+// c of one sequence from its SV chunk partials cp[0 .. SV) over a vocabulary
+// of V, with the weights (wH, wm, wp).  Called by all 32 lanes of one warp;
+// every lane returns c.
+__device__ __forceinline__ float conf_merge_c(const ConfPartial* __restrict__ cp, int SV, int V,
+                                              float wH, float wm, float wp) {
+  const int lane = threadIdx.x & 31;
   float M = -FLT_MAX;
-  for (int i = lane; i < s.SV; i += 32) M = fmaxf(M, cp[i].M);
+  for (int i = lane; i < SV; i += 32) M = fmaxf(M, __ldcg(&cp[i].M));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   FSum S{0.f, 0.f}, T{0.f, 0.f};
   Top2 tp{-FLT_MAX, -FLT_MAX, 0x7fffffff};
-  for (int i = lane; i < s.SV; i += 32) {
-    const ConfPartial p = cp[i];
+  for (int i = lane; i < SV; i += 32) {
+    const ConfPartial p = load_partial(cp + i);
     if (p.M > -FLT_MAX) {
       const float dm = p.M - M;
       const float f = expf(dm);
@@ -92,11 +187,19 @@ __device__ __forceinline__ void conf_merge_warp(const Shape& s, const Dev& d, in
   }
   const float Sv = S.hi + S.lo, Tv = T.hi + T.lo;
   const float H = logf(Sv) - Tv / Sv;
-  const float Hhat = H / logf((float)s.V);
+  const float Hhat = H / logf((float)V);
   const float m = tp.z1 - tp.z2;
   const float p1 = expf(tp.z1 - M) / Sv;
-  const float c = (float)s.wH * (1.0f - Hhat) + (float)s.wm * (1.0f / (1.0f + expf(-m))) +
-                  (float)s.wp * p1;
+  return wH * (1.0f - Hhat) + wm * (1.0f / (1.0f + expf(-m))) + wp * p1;
+}
+
+// Merges the partials of sequence b and publishes c (d.cval, conf_out) and
+// the budget of every layer of the sequence.  Called by all 32 lanes of one
+// warp.
+__device__ __forceinline__ void conf_merge_warp(const Shape& s, const Dev& d, int b, int32_t* budget,
+                                                float* conf_out) {
+  const int lane = threadIdx.x & 31;
+  const float c = conf_merge_c(d.conf + (size_t)b * s.SV, s.SV, s.V, (float)s.wH, (float)s.wm, (float)s.wp);
   const bool high = c >= (float)s.tau;   // compared in fp32, the precision of c
   for (int l = lane; l < s.L; l += 32) budget[(size_t)b * s.L + l] = high ? d.n_high[l] : d.n_low[l];
   if (lane == 0) {

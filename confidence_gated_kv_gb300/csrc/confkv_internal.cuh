@@ -122,6 +122,7 @@ struct Dev {
   int32_t* n_high; int32_t* n_low; // [l]
   ConfPartial* conf;               // [b][SV]
   double* cval;                    // [b] confidence of the current step
+  uint32_t* conf_done;             // [b] chunk partials of b done in the attention kernel (0 between steps)
   uint32_t* scratch;               // [l][b][S] selection keys / compaction pairs
   DevStats* stats;
   int32_t* status;                 // device status word (0 = ok)
@@ -188,10 +189,17 @@ int launch_prefill(const Shape& s, const Dev& d, const void* k, const void* v, l
 // step: the index of this decode step, or -1 for a step that takes it from
 // d.step_dev (a step captured into a graph, and every step while replays are
 // reserved); the select kernel of such a step advances d.step_dev.
+// conf: whether its blocks also reduce the logits to confidence partials
+// (otherwise the persistent attention kernel does).
 int launch_prestep(const Shape& s, const Dev& d, long long step, const float* logits,
-                   const void* k_new, const void* v_new, cudaStream_t stream);
+                   const void* k_new, const void* v_new, bool conf, cudaStream_t stream);
+// Writes out, and budget and conf_out (may be null) from the confidence
+// partials.  logits: null when the prestep kernel wrote the partials; else
+// (persistent kernel only) the epilogue warps reduce these logits to the
+// partials first and the last CTA to finish them merges.
 int launch_attention(const Shape& s, const Dev& d, const void* q, float* out, int32_t* budget,
-                     float* conf_out, int splits, int max_tokens, cudaStream_t stream);
+                     float* conf_out, const float* logits, int splits, int max_tokens,
+                     cudaStream_t stream);
 // Grid and cluster size of the attention launch for `splits` CTAs per unit
 // (the persistent kernel when 1, whose CTAs are not clustered).
 void attention_grid(const Shape& s, const Dev& d, int splits, int* grid, int* cluster);

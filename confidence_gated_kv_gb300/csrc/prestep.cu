@@ -168,9 +168,9 @@ template <int D, bool kDevStep>
 __global__ void __launch_bounds__(kConfThreads) prestep_kernel(Shape s, Dev d, long long step,
                                                                const float* __restrict__ logits,
                                                                const __half* __restrict__ k_new,
-                                                               const __half* __restrict__ v_new) {
+                                                               const __half* __restrict__ v_new,
+                                                               int nconf) {
   pdl_wait();
-  const int nconf = s.B * s.SV;
   if (blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(&d.stats->steps, 1ull);
   if ((int)blockIdx.x < nconf) {
     conf_block(s, d, logits, blockIdx.x / s.SV, blockIdx.x % s.SV);
@@ -182,20 +182,20 @@ __global__ void __launch_bounds__(kConfThreads) prestep_kernel(Shape s, Dev d, l
 }
 
 int launch_prestep(const Shape& s, const Dev& d, long long step, const float* logits,
-                   const void* k_new, const void* v_new, cudaStream_t stream) {
+                   const void* k_new, const void* v_new, bool conf, cudaStream_t stream) {
   const int units = s.L * s.B * s.Hkv;
-  const unsigned grid =
-      (unsigned)(s.B * s.SV + (units + kAppendUnitsPerBlock - 1) / kAppendUnitsPerBlock);
+  const int nconf = conf ? s.B * s.SV : 0;
+  const unsigned grid = (unsigned)(nconf + (units + kAppendUnitsPerBlock - 1) / kAppendUnitsPerBlock);
   const __half* kn = static_cast<const __half*>(k_new);
   const __half* vn = static_cast<const __half*>(v_new);
   const dim3 g(grid), blk(kConfThreads);
   cudaError_t e;
   if (step >= 0)
-    e = s.D == 128 ? launch_pdl(prestep_kernel<128, false>, g, blk, 0, stream, s, d, step, logits, kn, vn)
-                   : launch_pdl(prestep_kernel<64, false>, g, blk, 0, stream, s, d, step, logits, kn, vn);
+    e = s.D == 128 ? launch_pdl(prestep_kernel<128, false>, g, blk, 0, stream, s, d, step, logits, kn, vn, nconf)
+                   : launch_pdl(prestep_kernel<64, false>, g, blk, 0, stream, s, d, step, logits, kn, vn, nconf);
   else
-    e = s.D == 128 ? launch_pdl(prestep_kernel<128, true>, g, blk, 0, stream, s, d, step, logits, kn, vn)
-                   : launch_pdl(prestep_kernel<64, true>, g, blk, 0, stream, s, d, step, logits, kn, vn);
+    e = s.D == 128 ? launch_pdl(prestep_kernel<128, true>, g, blk, 0, stream, s, d, step, logits, kn, vn, nconf)
+                   : launch_pdl(prestep_kernel<64, true>, g, blk, 0, stream, s, d, step, logits, kn, vn, nconf);
   return e == cudaSuccess ? 0 : -1;
 }
 

@@ -321,6 +321,8 @@ def run_ours(args):
         hout = cache.host_outputs()
         h2d = hq[0].numel() * hq[0].element_size() + 2 * hk[0].numel() * 2 + hl[0].numel() * 4
         d2h = sum(x.numel() * x.element_size() for x in hout.values())
+        for s in range(4):   # untimed: first calls create the library's second stream
+            cache.step_host(hq[s % R], hk[s % R], hv[s % R], hl[s % R], hout)
         torch.cuda.synchronize()
         e0 = time.perf_counter()
         for s in range(args.e2e_steps):
@@ -515,7 +517,7 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=4003)
     ap.add_argument("--pool", type=int, default=16)
-    ap.add_argument("--e2e-steps", type=int, default=32)
+    ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--compaction", default="tailfill", choices=["tailfill", "ordered"],
                     help="INT8 compaction: tail fill (default) or the order-preserving ablation")

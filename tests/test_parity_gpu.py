@@ -240,10 +240,13 @@ def test_gpt2_small_batch8_pyramid_prefix():
     p.compare_states()
 
 
+@pytest.mark.parametrize("ctas", [0, 3])
 @pytest.mark.parametrize("pinned", [True, False, "mixed"])
-def test_host_buffer_step_matches_device_step(pinned):
+def test_host_buffer_step_matches_device_step(pinned, ctas):
     # pinned buffers take the mapped mode (kernels read and write host memory
-    # in place); pageable ones, or a mix, the staged copies
+    # in place); pageable ones, or a mix, the staged copies.  Without a cap
+    # the 8 units take the split-K kernel; a cap of 3 CTAs the persistent
+    # kernel, which then reads q and reduces the logits from host memory.
     w = Workload(name="t_host", B=2, L=2, Hq=8, Hkv=2, d=128, V=3000, T0=100, steps=5,
                  n_high=(40, 40), n_low=(64, 64), P=8, W=16, q_dtype="bf16")
     k, v = prefill_batch(w, 16, "cpu")
@@ -251,6 +254,9 @@ def test_host_buffer_step_matches_device_step(pinned):
     b = ck.Cache(ck.config_from_workload(w))
     a.prefill(k.cuda(), v.cuda(), [w.T0] * w.B)
     b.prefill(k.cuda(), v.cuda(), [w.T0] * w.B)
+    a.set_attention_ctas(ctas)
+    b.set_attention_ctas(ctas)
+    assert (b.attention_plan()[0] == 1) == (ctas == 3)
     hout = b.host_outputs(pin=pinned is not False)
     pin_in = pinned is True
     for s in range(5):
@@ -262,6 +268,9 @@ def test_host_buffer_step_matches_device_step(pinned):
         assert b.stats()["host_h2d_bytes"] == sum(x.numel() * x.element_size() for x in (q, kn, vn, lg))
         assert torch.equal(o["out"].cpu(), hout["out"])
         assert torch.equal(o["budget"].cpu(), hout["budget"])
+        # mapped steps on the persistent kernel reduce the logits in the
+        # attention kernel (another summation order): c agrees to fp32 rounding
+        assert torch.allclose(o["confidence"].cpu(), hout["confidence"], rtol=0, atol=1e-6)
         assert torch.equal(o["n_evicted"].cpu(), hout["n_evicted"])
         n = o["n_evicted"].cpu()
         for l in range(w.L):

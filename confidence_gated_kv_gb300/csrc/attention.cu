@@ -114,8 +114,11 @@ __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], 
 //    every score of a query row, which is subtracted once per block in fp32
 //    (the QK accumulator restarts at zero every block).
 //  - V operand: also used as is; the PV accumulator gathers 1152 * sum p on
-//    top of sum p * code, removed once per ring write (ws_scale_v) from the
-//    row sum of p that the softmax keeps anyway.
+//    top of sum p * code.  That bias is subtracted every 16 INT8 blocks of a
+//    warp and at the end of its INT8 blocks (ws_flush_v_bias), from the row
+//    sum of p that the softmax keeps anyway; left to the end of a long INT8
+//    region it would grow the accumulator ~1000-fold above the result and
+//    the fp32 tensor-core sums would lose ~3e-3 over 8K tokens per warp.
 __device__ __forceinline__ void u8x4_to_h2x2_biased(uint32_t w, uint32_t& b0, uint32_t& b1) {
   b0 = __byte_perm(w, 0x64646464u, 0x5140);
   b1 = __byte_perm(w, 0x64646464u, 0x5342);
@@ -197,10 +200,10 @@ __device__ __forceinline__ float make_q_frag(uint32_t (&aq)[D / 16][4], const vo
 // m_run only moves when the block maximum exceeds it by more than 8 (log2
 // units), so most blocks skip rescaling the accumulator; p = 2^(s - m_run)
 // then stays below 2^8, well inside fp16.
-template <int D>
+template <int D, bool kFlush>
 __device__ __forceinline__ void softmax_block(float (&sc4)[2][2], const bool (&valid)[2][2],
                                               int G, int g, float& m_run, float& l_run,
-                                              float (&acc)[D / 8][4], float* sc_dst,
+                                              float& l_fl, float (&acc)[D / 8][4], float* sc_dst,
                                               uint32_t (&pa)[4], float* sc_regs) {
   float mloc = -INFINITY;
 #pragma unroll
@@ -219,6 +222,7 @@ __device__ __forceinline__ void softmax_block(float (&sc4)[2][2], const bool (&v
     const float corr = move ? (m_run == -INFINITY ? 0.f : ex2(m_run - mloc)) : 1.0f;
     if (move) m_run = mloc;
     l_run *= corr;
+    if (kFlush) l_fl *= corr;
 #pragma unroll
     for (int j = 0; j < D / 8; ++j) {
       acc[j][0] *= corr; acc[j][1] *= corr; acc[j][2] *= corr; acc[j][3] *= corr;
@@ -273,7 +277,9 @@ struct WarpState {
   uint32_t aq[D / 16][4];   // query A fragments (INT8 version, then FP16 version)
   float acc[D / 8][4];      // PV accumulators: rows g (hi P) and g + 8 (lo P)
   float m_run, l_run;       // reference maximum (log2 units) and lane-partial sum
+  float l_flushed;          // part of l_run whose INT8 V bias is already removed
   float qoffset;            // 1152 * sum(q') of the row (INT8 K operand offset)
+  int n8blk;                // INT8 blocks done by this warp in this unit
   bool in_ring;
 };
 
@@ -285,19 +291,38 @@ __device__ __forceinline__ void ws_begin(WarpState<D>& w, const void* q, size_t 
   for (int j = 0; j < D / 8; ++j) w.acc[j][0] = w.acc[j][1] = w.acc[j][2] = w.acc[j][3] = 0.f;
   w.m_run = -INFINITY;
   w.l_run = 0.f;
+  w.l_flushed = 0.f;
+  w.n8blk = 0;
   w.in_ring = false;
+}
+
+// Removes the INT8 V bias 1152 * sum p that the accumulator gathered since
+// the last flush.  The INT8 V operand enters the products as fp16
+// 1152 + code (two byte permutes, no subtraction).  l_run - l_flushed is this
+// lane's sum of the p since then (both are rescaled with the accumulator):
+// the four lanes of a row add up the row's bias.  The high and low parts of
+// P sit in rows g and g + 8; the bias of both is removed from row g, whose
+// sum with row g + 8 is the output.
+template <int D>
+__device__ __forceinline__ void ws_flush_v_bias(WarpState<D>& w) {
+  float l = w.l_run - w.l_flushed;
+  l += __shfl_xor_sync(0xffffffffu, l, 1);
+  l += __shfl_xor_sync(0xffffffffu, l, 2);
+  const float bias = 1152.0f * l;
+#pragma unroll
+  for (int j = 0; j < D / 8; ++j) {
+    w.acc[j][0] -= bias;
+    w.acc[j][1] -= bias;
+  }
+  w.l_flushed = w.l_run;
 }
 
 // Multiply what the INT8 codes accumulated by the per-channel V scale.
 template <int D>
 __device__ __forceinline__ void ws_scale_v(WarpState<D>& w, const float* sVu, int t) {
-  // The INT8 V operand entered the products as fp16 1152 + code (two byte
-  // permutes, no subtraction), so the accumulator holds sum p (1152 + code).
-  // l_run is, up to this point, this lane's sum of the same p (rescaled with
-  // the accumulator): the four lanes of a row add up the row's bias.  The
-  // high and low parts of P sit in rows g and g + 8; the bias of both is
-  // removed from row g, whose sum with row g + 8 is the output.
-  float l = w.l_run;
+  // the bias of the blocks since the last flush (all of them without
+  // flushes), then the scale; called once per unit, so l_flushed is left
+  float l = w.l_run - w.l_flushed;
   l += __shfl_xor_sync(0xffffffffu, l, 1);
   l += __shfl_xor_sync(0xffffffffu, l, 2);
   const float bias = 1152.0f * l;
@@ -323,7 +348,9 @@ __device__ __forceinline__ void ws_to_ring(WarpState<D>& w, const void* q, size_
 }
 
 // One INT8 block at shared-memory addresses kb / vb (16*D bytes each).
-template <int D>
+// kFlush: remove the INT8 V bias every 16 blocks of the warp (long INT8
+// regions); otherwise it is removed once, when the warp leaves them.
+template <int D, bool kFlush>
 __device__ __forceinline__ void int8_block(WarpState<D>& w, uint32_t kb, uint32_t vb, int blk,
                                            int n8, int G, int g, int t, int lane, float* sc_dst,
                                            float* sc_regs = nullptr) {
@@ -352,13 +379,15 @@ __device__ __forceinline__ void int8_block(WarpState<D>& w, uint32_t kb, uint32_
     valid[nt][1] = full || tok + 1 < n8;
   }
   uint32_t pa[4];
-  softmax_block<D>(sc4, valid, G, g, w.m_run, w.l_run, w.acc, sc_dst, pa, sc_regs);
+  softmax_block<D, kFlush>(sc4, valid, G, g, w.m_run, w.l_run, w.l_flushed, w.acc, sc_dst, pa,
+                           sc_regs);
 #pragma unroll
   for (int j = 0; j < D / 8; ++j) {
     uint32_t b0, b1;
-    u8x4_to_h2x2_biased(comp(vw[j >> 2], j & 3), b0, b1);   // 1152 + code: bias removed in ws_scale_v
+    u8x4_to_h2x2_biased(comp(vw[j >> 2], j & 3), b0, b1);   // 1152 + code: bias flushed below
     mma16816(w.acc[j], pa, b0, b1);
   }
+  if (kFlush && (++w.n8blk & 15) == 0) ws_flush_v_bias<D>(w);
 }
 
 // One FP16 ring block at kb / vb (32*D bytes each); posb = the block's 16
@@ -385,7 +414,7 @@ __device__ __forceinline__ void ring_block(WarpState<D>& w, uint32_t kb, uint32_
     sc4[nt][1] = (c[1] + c[3]) * kQPreInv;
   }
   uint32_t pa[4];
-  softmax_block<D>(sc4, valid, G, g, w.m_run, w.l_run, w.acc, sc_dst, pa, sc_regs);
+  softmax_block<D, false>(sc4, valid, G, g, w.m_run, w.l_run, w.l_flushed, w.acc, sc_dst, pa, sc_regs);
 #pragma unroll
   for (int r = 0; r < D / 16; ++r) {
     const uint4 w4 = lds128(vb + r * 512 + lane * 16);
@@ -541,8 +570,8 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(Shape s, Dev d,
       if (!ring) {
         if (warp < nb) {
           const int blk = first + warp;
-          int8_block<D>(ws, stage + warp * 16 * D, stage + kHalf + warp * 16 * D, blk, n8, G, g, t,
-                        lane, sc + g * chunk_tok + (blk - blk0) * 16 + 2 * t);
+          int8_block<D, true>(ws, stage + warp * 16 * D, stage + kHalf + warp * 16 * D, blk, n8, G, g,
+                              t, lane, sc + g * chunk_tok + (blk - blk0) * 16 + 2 * t);
         }
       } else {
         const int jb = warp - 2 * ((i - sch.n8st) & 1);
@@ -735,7 +764,7 @@ struct RingPos {
   }
 };
 
-template <int D>
+template <int D, bool kFlush>
 __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
     Shape s, Dev d, const void* __restrict__ q, float* __restrict__ out,
     int32_t* __restrict__ budget, float* __restrict__ conf_out, const float* __restrict__ logits,
@@ -986,6 +1015,8 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
     for (int j = 0; j < D / 8; ++j) ws.acc[j][0] = ws.acc[j][1] = ws.acc[j][2] = ws.acc[j][3] = 0.f;
     ws.m_run = -INFINITY;
     ws.l_run = 0.f;
+    ws.l_flushed = 0.f;
+    ws.n8blk = 0;
     ws.in_ring = false;
     float sc4buf[4];
     bool ok = true;
@@ -1000,8 +1031,8 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
         if (warp < nb) {
           const int blk = first + warp;
           tok0 = blk * 16;
-          int8_block<D>(ws, stage + warp * 16 * D, stage + kHalf + warp * 16 * D, blk, n8, G, g, t,
-                        lane, nullptr, sc4buf);
+          int8_block<D, kFlush>(ws, stage + warp * 16 * D, stage + kHalf + warp * 16 * D, blk, n8, G, g,
+                                t, lane, nullptr, sc4buf);
         }
       } else {
         // a ring stage holds 2 FP16 blocks: warps 0-1 take the even ring
@@ -1127,7 +1158,11 @@ void attention_grid(const Shape& s, const Dev& d, int splits, int* grid_out, int
     *cluster_out = splits;
     return;
   }
-  int grid = units < 2 * num_sms() ? units : 2 * num_sms();
+  // one unit per CTA, or two CTAs per SM; when the units fill between one
+  // and two such rounds, half of them per round (both rounds full: the
+  // 512 units of 4K tokens took 0.118 ms on 256 CTAs, 0.123 ms on 304)
+  const int full = 2 * num_sms();
+  int grid = units <= full ? units : units < 2 * full ? (units + 1) / 2 : full;
   if (grid > d.score_ctas) grid = d.score_ctas;
   if (d.attn_ctas > 0 && grid > d.attn_ctas) grid = d.attn_ctas;
   *grid_out = grid;
@@ -1159,6 +1194,10 @@ int launch_selftest_timeout(const Dev& d, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
+// INT8 tokens per unit above which the persistent kernel flushes the INT8 V
+// bias as it goes (see launch_d)
+constexpr int kFlushTokens = 8192;
+
 template <int D>
 static int launch_d(const Shape& s, const Dev& d, const void* q, float* out, int32_t* budget,
                     float* conf_out, const float* logits, int splits, int max_tokens,
@@ -1168,18 +1207,25 @@ static int launch_d(const Shape& s, const Dev& d, const void* q, float* out, int
   if (smem > attention_max_smem()) return -1;
   const int units = s.L * s.B * s.Hkv;
   if (splits == 1) {
-    static bool configured = false;
-    if (!configured) {
-      if (cudaFuncSetAttribute(attention_persistent_kernel<D>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               attention_max_smem()) != cudaSuccess)
+    // Units whose INT8 region can exceed 8192 tokens take the instance that
+    // removes the INT8 V bias every 16 blocks of a warp.  The error that
+    // this avoids grows with a warp's INT8 blocks: 2.7e-3 max-abs at ~500
+    // blocks per warp (32K-token units), below 7e-4 up to 128.  Shorter
+    // units keep the other instance: the flush state costs 2 % of a kernel
+    // at its register limit (0.292 against 0.285 ms on the Qwen-32B shape).
+    static bool configured[2] = {false, false};
+    const bool flush = max_tokens - s.WR > kFlushTokens;
+    auto kern = flush ? attention_persistent_kernel<D, true> : attention_persistent_kernel<D, false>;
+    if (!configured[flush]) {
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, attention_max_smem()) !=
+          cudaSuccess)
         return -1;
-      configured = true;
+      configured[flush] = true;
     }
     int grid = 0, cluster = 0;
     attention_grid(s, d, 1, &grid, &cluster);
-    return launch_pdl(attention_persistent_kernel<D>, dim3(grid), dim3(kPThreads), (size_t)smem, stream,
-                      s, d, q, out, budget, conf_out, logits, stages_persistent(s)) == cudaSuccess
+    return launch_pdl(kern, dim3(grid), dim3(kPThreads), (size_t)smem, stream, s, d, q, out, budget,
+                      conf_out, logits, stages_persistent(s)) == cudaSuccess
                ? 0
                : -1;
   }

@@ -83,7 +83,7 @@ def test_qwen14b_shape_sampled_units():
     _sampled_fullsize("qwen14b", 4002, steps=3, n_units=4, expect_splits=lambda sp: sp == 1)
 
 
-def test_needle32k_first_steps_split_path():
-    # 32768-token prefill, first step evicts ~28.7K entries per unit through
-    # the split-K cluster kernel
-    _sampled_fullsize("needle32k", 4004, steps=2, n_units=3, expect_splits=lambda sp: sp > 1)
+def test_needle32k_first_steps():
+    # 32768-token prefill, first step evicts ~28.7K entries per unit; 512
+    # units of up to 32K tokens each on the persistent kernel
+    _sampled_fullsize("needle32k", 4004, steps=2, n_units=3, expect_splits=lambda sp: sp == 1)

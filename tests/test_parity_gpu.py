@@ -95,6 +95,25 @@ def test_split_k_cluster_path_and_large_first_eviction():
     assert p.flags.evictions >= 2000 - 600
 
 
+def test_long_int8_units_on_the_persistent_kernel():
+    # One unit per sequence with a 32K-token INT8 region on the persistent
+    # kernel (a cap of 2 CTAs keeps these two units off the split-K path):
+    # every consumer warp runs ~500 INT8 blocks, so the kernel instance that
+    # removes the INT8 V bias as it goes is launched.  Needle queries keep the
+    # softmax flat.  With the bias left to the end of the INT8 blocks the
+    # output was off by 2.7e-3 on such units.
+    w = Workload(name="t_long", B=2, L=1, Hq=5, Hkv=1, d=128, V=2000, T0=32768, steps=3,
+                 n_high=(40000,), n_low=(40000,), P=8, W=64, q_dtype="bf16", needle=True)
+    p = Pair(w, 23)
+    p.cache.set_attention_ctas(2)
+    assert p.cache.attention_plan()[0] == 1
+    assert p.cache.attention_grid() == (2, 1)
+    for s in range(3):
+        q, kn, vn, lg = step_inputs(w, 23, s)
+        p.step(q, kn, vn, lg)
+    assert p.flags.max_out_err <= 2e-3
+
+
 def test_full_kv_long_ring_on_the_persistent_kernel():
     # full KV: no eviction and an FP16 window longer than every cache, so the
     # ring (1120 slots) is too long for the unit header and the persistent

@@ -164,9 +164,10 @@ class OracleSample:
         return 1.0 / (wall / max(done, 1) * self.w.L * self.w.B)
 
 
-def cpu_baseline(w, seed: int, units: int = 8, steps: int = 24):
+def cpu_baseline(w, seed: int, units: int = 8, steps: int = 120):
     """Oracle steps/s of the whole workload, extrapolated from a bounded
-    sample of unit-steps timed on the host cores."""
+    sample of unit-steps timed on the host cores (about 10 s of oracle work
+    on the Qwen-32B shape)."""
     smp = OracleSample(w, seed, units)
     done, wall, cpu = smp.run(steps)
     return {

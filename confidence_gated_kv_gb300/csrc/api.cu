@@ -268,14 +268,17 @@ static int plan_attention_for(const confkv_ctx* ctx, long long n8_bound, int* sp
   const int nbT = max_tokens / 16;
   int splits = 1;
   // Units split over CTA clusters only while there are fewer units than
-  // persistent CTAs (two per SM); then enough CTAs to fill the GPU a few
-  // times over, at least 4 blocks per CTA, and no more CTAs than the caller's
-  // cap on the attention grid.  From one unit per persistent CTA upwards,
-  // whole units on the persistent kernel are faster (512 units of 4K tokens:
-  // 0.123 ms against 0.176 ms on 2-CTA clusters).
+  // persistent CTAs (two per SM) and each CTA keeps at least 64 blocks
+  // (1024 tokens); then enough CTAs to fill the GPU a few times over, and no
+  // more CTAs than the caller's cap on the attention grid.  Below that, the
+  // cluster's launch and merge cost more than the shorter stream saves:
+  // 144 units of ~500 tokens took 0.0165 ms as whole units against 0.025 ms
+  // on 8-CTA clusters, and from one unit per persistent CTA upwards whole
+  // units are faster too (512 units of 4K tokens: 0.123 against 0.176 ms on
+  // 2-CTA clusters).
   const long long cap = ctx->d.attn_ctas;
   const bool few = units < 2LL * kNumSMs;
-  while (few && splits < kMaxSplits && units * splits < 4LL * kNumSMs && nbT / (splits * 2) >= 4 &&
+  while (few && splits < kMaxSplits && units * splits < 4LL * kNumSMs && nbT / (splits * 2) >= 64 &&
          (cap == 0 || units * splits * 2 <= cap))
     splits *= 2;
   while (splits < kMaxSplits && attention_smem_bytes(s, splits, max_tokens) > attention_max_smem())

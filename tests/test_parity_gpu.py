@@ -75,11 +75,12 @@ def test_persistent_kernel_several_units_per_cta_under_a_cta_cap():
     assert p.flags.max_out_err <= 2e-3
 
 
-def test_split_k_cluster_path_and_large_first_eviction():
-    # two units of 4000 tokens on 2-CTA clusters (at least 1024 tokens per
-    # CTA); the launch shape follows the host's bound on the cache length
-    # (the loose budget), so the confident step's cut to 1500 keeps it
-    w = Workload(name="t_split", B=1, L=1, Hq=8, Hkv=2, d=128, V=4000, T0=4000, steps=6,
+@pytest.mark.parametrize("d, Hq, Hkv", [(128, 8, 2), (64, 4, 4)])
+def test_split_k_cluster_path_and_large_first_eviction(d, Hq, Hkv):
+    # units of 4000 tokens on 2-CTA clusters (at least 1024 tokens per CTA);
+    # the launch shape follows the host's bound on the cache length (the
+    # loose budget), so the confident step's cut to 1500 keeps it
+    w = Workload(name="t_split", B=1, L=1, Hq=Hq, Hkv=Hkv, d=d, V=4000, T0=4000, steps=6,
                  n_high=(1500,), n_low=(3000,), P=16, W=64, q_dtype="bf16", heavy_count=10,
                  heavy_factor=3.0)
     p = Pair(w, 14)

@@ -1138,14 +1138,16 @@ int attention_smem_bytes(const Shape& s, int splits, int max_tokens) {
 
 int attention_persistent_ctas();
 
+// SMs of the current device (152 on GB300), recorded per device
 static int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      n = 152;
-  }
+  static int sms[kMaxDevices] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const bool known = dev >= 0 && dev < kMaxDevices;
+  if (known && sms[dev] > 0) return sms[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+  if (known) sms[dev] = n;
   return n;
 }
 
@@ -1213,15 +1215,10 @@ static int launch_d(const Shape& s, const Dev& d, const void* q, float* out, int
     // blocks per warp (32K-token units), below 7e-4 up to 128.  Shorter
     // units keep the other instance: the flush state costs 2 % of a kernel
     // at its register limit (0.292 against 0.285 ms on the Qwen-32B shape).
-    static bool configured[2] = {false, false};
+    static int configured[2][kMaxDevices] = {};
     const bool flush = max_tokens - s.WR > kFlushTokens;
     auto kern = flush ? attention_persistent_kernel<D, true> : attention_persistent_kernel<D, false>;
-    if (!configured[flush]) {
-      if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, attention_max_smem()) !=
-          cudaSuccess)
-        return -1;
-      configured[flush] = true;
-    }
+    if (ensure_smem(kern, attention_max_smem(), configured[flush]) != cudaSuccess) return -1;
     int grid = 0, cluster = 0;
     attention_grid(s, d, 1, &grid, &cluster);
     return launch_pdl(kern, dim3(grid), dim3(kPThreads), (size_t)smem, stream, s, d, q, out, budget,
@@ -1229,13 +1226,8 @@ static int launch_d(const Shape& s, const Dev& d, const void* q, float* out, int
                ? 0
                : -1;
   }
-  static bool configured_split = false;
-  if (!configured_split) {
-    if (cudaFuncSetAttribute(attention_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             attention_max_smem()) != cudaSuccess)
-      return -1;
-    configured_split = true;
-  }
+  static int configured_split[kMaxDevices] = {};
+  if (ensure_smem(attention_kernel<D>, attention_max_smem(), configured_split) != cudaSuccess) return -1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)units * splits);
   cfg.blockDim = dim3(kAttnThreads);

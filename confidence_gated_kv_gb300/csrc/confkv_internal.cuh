@@ -179,6 +179,24 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
+
+// Devices a process can use with the per-device records below.
+constexpr int kMaxDevices = 64;
+
+// Raises `kernel`'s dynamic shared memory limit to at least `bytes` on the
+// current device.  cudaFuncSetAttribute acts on the current device only, so
+// each launcher keeps its own record `done` of the limit set per device.
+template <typename... KArgs>
+inline cudaError_t ensure_smem(void (*kernel)(KArgs...), int bytes, int (&done)[kMaxDevices]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool known = dev >= 0 && dev < kMaxDevices;
+  if (known && done[dev] >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && known) done[dev] = bytes;
+  return e;
+}
 #endif
 
 // ---------------------------------------------------------------------------

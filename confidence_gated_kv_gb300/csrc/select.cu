@@ -766,13 +766,10 @@ static SelSmem plan_select(const Shape& s) {
 template <int D, bool kSmemKeys, bool kDevStep, bool kOrdered>
 static int launch_select_t(const Shape& s, const Dev& d, long long step, int32_t* evicted_pos,
                            int32_t* n_evicted, const SelSmem& p, cudaStream_t stream) {
-  static int configured = 48 * 1024;
-  if (p.bytes > configured) {
-    if (cudaFuncSetAttribute(select_kernel<D, kSmemKeys, kDevStep, kOrdered>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, p.bytes) != cudaSuccess)
-      return -1;
-    configured = p.bytes;
-  }
+  static int configured[kMaxDevices] = {};
+  if (p.bytes > 48 * 1024 &&
+      ensure_smem(select_kernel<D, kSmemKeys, kDevStep, kOrdered>, p.bytes, configured) != cudaSuccess)
+    return -1;
   return launch_pdl(select_kernel<D, kSmemKeys, kDevStep, kOrdered>, dim3(s.L * s.B), dim3(kSelThreads),
                     (size_t)p.bytes, stream, s, d, step, evicted_pos, n_evicted, p) == cudaSuccess
              ? 0

@@ -30,3 +30,10 @@ def test_compare_policies_are_the_pages_baselines():
     import pytest
     with pytest.raises(ValueError):
         bench.variant_workload(w, "h2o", 10)
+
+
+def test_attention_traffic_ratio_is_read_from_the_summary():
+    # `traffic` = this ratio x the timed launches' own algorithmic bytes
+    r = bench._traffic_ratio_from_profiles("attention_kernel_qwen32b")
+    assert r is not None and 1.0 <= r < 1.2
+    assert bench._traffic_ratio_from_profiles("attention_kernel_no_such_workload") is None

@@ -11,6 +11,7 @@ from .binding import (  # noqa: F401
     ConfkvError,
     block_offset,
     config_from_workload,
+    launch_plan,
     lib,
     make_config,
     status_string,

@@ -77,6 +77,9 @@ def lib() -> ctypes.CDLL:
         vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
         sigs = {
             "confkv_workspace_bytes": (ctypes.c_int, [ctypes.POINTER(Config), ctypes.POINTER(sz)]),
+            "confkv_launch_plan": (ctypes.c_int, [ctypes.POINTER(Config), ctypes.c_int64, i32,
+                                                  ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                                  ctypes.POINTER(i32)]),
             "confkv_create": (ctypes.c_int, [ctypes.POINTER(Config), vp, sz, ctypes.POINTER(vp)]),
             "confkv_destroy": (None, [vp]),
             "confkv_prefill": (ctypes.c_int, [vp, vp, vp, vp, i64, vp]),
@@ -189,6 +192,15 @@ def workspace_bytes(cfg: Config) -> int:
     n = ctypes.c_size_t(0)
     _check(lib().confkv_workspace_bytes(ctypes.byref(cfg), ctypes.byref(n)), "confkv_workspace_bytes")
     return int(n.value)
+
+
+def launch_plan(cfg: Config, n8_bound: int, attn_ctas: int = 0):
+    """(CTAs per unit, grid CTAs, cluster size) of the attention launch for a
+    bound `n8_bound` on the INT8 entries per (layer, sequence); host only."""
+    sp, g, c = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().confkv_launch_plan(ctypes.byref(cfg), int(n8_bound), int(attn_ctas), ctypes.byref(sp),
+                                    ctypes.byref(g), ctypes.byref(c)), "confkv_launch_plan")
+    return int(sp.value), int(g.value), int(c.value)
 
 
 class Cache:

@@ -260,9 +260,10 @@ int confkv_prefill(confkv_ctx* ctx, const int32_t* prefill_len, const void* k, c
 }
 
 // Launch shape of the attention kernel for an INT8 bound.
-static int plan_attention_for(const confkv_ctx* ctx, long long n8_bound, int* splits_out,
-                              int* max_tokens_out) {
-  const Shape& s = ctx->s;
+// Attention launch for shape s, a bound n8_bound on the INT8 entries of any
+// (layer, sequence) and a cap on the persistent grid (0 = none).
+static int plan_attention_shape(const Shape& s, long long attn_ctas, long long n8_bound, int* splits_out,
+                                int* max_tokens_out) {
   const int max_tokens = (int)align_up((size_t)n8_bound, 16) + s.WR;
   const long long units = (long long)s.L * s.B * s.Hkv;
   const int nbT = max_tokens / 16;
@@ -276,7 +277,7 @@ static int plan_attention_for(const confkv_ctx* ctx, long long n8_bound, int* sp
   // on 8-CTA clusters, and from one unit per persistent CTA upwards whole
   // units are faster too (512 units of 4K tokens: 0.123 against 0.176 ms on
   // 2-CTA clusters).
-  const long long cap = ctx->d.attn_ctas;
+  const long long cap = attn_ctas;
   const bool few = units < 2LL * kNumSMs;
   while (few && splits < kMaxSplits && units * splits < 4LL * kNumSMs && nbT / (splits * 2) >= 64 &&
          (cap == 0 || units * splits * 2 <= cap))
@@ -286,6 +287,31 @@ static int plan_attention_for(const confkv_ctx* ctx, long long n8_bound, int* sp
   if (attention_smem_bytes(s, splits, max_tokens) > attention_max_smem()) return CONFKV_ECAPACITY;
   *splits_out = splits;
   *max_tokens_out = max_tokens;
+  return CONFKV_OK;
+}
+
+static int plan_attention_for(const confkv_ctx* ctx, long long n8_bound, int* splits_out,
+                              int* max_tokens_out) {
+  return plan_attention_shape(ctx->s, ctx->d.attn_ctas, n8_bound, splits_out, max_tokens_out);
+}
+
+int confkv_launch_plan(const confkv_config* cfg, int64_t n8_bound, int32_t attn_ctas, int32_t* splits,
+                       int32_t* ctas, int32_t* cluster) {
+  if (!splits || !ctas || !cluster || !valid_config(cfg) || n8_bound < 0 || attn_ctas < 0)
+    return CONFKV_EINVAL;
+  const Shape s = make_shape(cfg);
+  if (n8_bound > s.cap) return CONFKV_EINVAL;
+  int sp = 0, mt = 0;
+  const int r = plan_attention_shape(s, attn_ctas, n8_bound, &sp, &mt);
+  if (r != CONFKV_OK) return r;
+  Dev d{};
+  d.score_ctas = attention_persistent_ctas();
+  d.attn_ctas = attn_ctas;
+  int g = 0, c = 0;
+  attention_grid(s, d, sp, &g, &c);
+  *splits = sp;
+  *ctas = g;
+  *cluster = c;
   return CONFKV_OK;
 }
 

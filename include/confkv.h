@@ -304,6 +304,22 @@ int confkv_set_attention_ctas(confkv_ctx* ctx, int32_t ctas);
  * `splits` CTAs per unit. */
 int confkv_attention_grid(confkv_ctx* ctx, int32_t* ctas, int32_t* cluster);
 
+/* The attention launch a step would take, planned on the host alone (no
+ * context; nothing runs on a GPU): for configuration `cfg`, a bound
+ * `n8_bound` on the INT8 entries of any (layer, sequence) and a cap
+ * `attn_ctas` on the persistent grid (0 = none, as confkv_set_attention_ctas),
+ * `splits` CTAs per (layer, sequence, KV head) unit (1 = the persistent
+ * kernel) and a grid of `ctas` CTAs in clusters of `cluster`.  A context
+ * plans each step the same way with its own host bound on n8 (the largest
+ * prefill minus W, then at most the largest budget).  The SM count is the
+ * current device's, 152 (GB300) when none can be queried.  CONFKV_EINVAL
+ * for a null argument, an invalid configuration, a negative bound or cap,
+ * or a bound above cap; CONFKV_ECAPACITY when no launch fits in shared
+ * memory.  The pages give no counterpart: it exposes this library's launch
+ * planning. */
+int confkv_launch_plan(const confkv_config* cfg, int64_t n8_bound, int32_t attn_ctas, int32_t* splits,
+                       int32_t* ctas, int32_t* cluster);
+
 /* Byte offset of (token tau in [0,16), channel c) inside one 16-token block of
  * the device layout: kind 0 = INT8 K, 1 = INT8 V, 2 = FP16 K, 3 = FP16 V.
  * Host-only helper for tests of the interleave; -1 for bad arguments. */

@@ -138,3 +138,46 @@ def test_status_bits_match_the_kernels():
 def test_both_compaction_layouts_are_valid():
     for c in (binding.COMPACT_TAIL_FILL, binding.COMPACT_ORDERED):
         assert ck.workspace_bytes(_cfg(compaction=c)) > 0
+
+
+# ------------------------------------------------------------ launch planning
+
+@pytest.mark.parametrize("name, n8, expect", [
+    # 4096 / 1536 / 1152 units: the persistent kernel, two CTAs per SM
+    ("qwen32b", 2048, (1, 304, 1)),
+    ("qwen14b", 8192 - 256, (1, 304, 1)),
+    ("gpt2_b8_pyramid", 768, (1, 304, 1)),
+    # 512 units: two rounds of 256 CTAs, at the 32K-token first step too
+    ("needle32k", 32768 - 256, (1, 256, 1)),
+    ("needle32k", 4096 - 256, (1, 256, 1)),
+    # 144 units of ~600 tokens: one whole unit per CTA, no clusters
+    ("gpt2_b1", 600 - 64, (1, 144, 1)),
+])
+def test_launch_plan_of_each_workload(name, n8, expect):
+    w = WORKLOADS[name]
+    assert ck.launch_plan(ck.config_from_workload(w), n8) == expect
+
+
+def test_launch_plan_splits_only_long_units_of_few_sequences():
+    from workload import Workload
+    w = Workload(name="t", B=1, L=1, Hq=8, Hkv=2, d=128, V=4000, T0=4000, steps=1,
+                 n_high=(1500,), n_low=(3000,), P=16, W=64)
+    cfg = ck.config_from_workload(w)
+    # 2 units of ~4000 tokens: 2-CTA clusters keep 1024+ tokens per CTA
+    assert ck.launch_plan(cfg, 4000 - 64) == (2, 4, 2)
+    # ~1500 tokens: too short to split
+    assert ck.launch_plan(cfg, 1500) == (1, 2, 1)
+    # a cap of 2 CTAs keeps whole units on the persistent kernel
+    assert ck.launch_plan(cfg, 4000 - 64, attn_ctas=2) == (1, 2, 1)
+
+
+def test_launch_plan_cap_and_bad_arguments():
+    cfg = ck.config_from_workload(WORKLOADS["qwen32b"])
+    assert ck.launch_plan(cfg, 2048, attn_ctas=100) == (1, 100, 1)
+    L = ck.lib()
+    out = [ctypes.c_int32() for _ in range(3)]
+    refs = [ctypes.byref(x) for x in out]
+    assert L.confkv_launch_plan(ctypes.byref(cfg), -1, 0, *refs) == binding.EINVAL
+    assert L.confkv_launch_plan(ctypes.byref(cfg), 2048, -1, *refs) == binding.EINVAL
+    assert L.confkv_launch_plan(ctypes.byref(cfg), cfg.cap + 1, 0, *refs) == binding.EINVAL
+    assert L.confkv_launch_plan(None, 2048, 0, *refs) == binding.EINVAL

@@ -282,7 +282,12 @@ int confkv_profile_read(confkv_ctx* ctx, double* ms_prestep, double* ms_attentio
                         double* ms_select, int32_t* steps);
 
 /* Attention launch shape chosen for the next step: CTAs per (layer, sequence,
- * KV head) and dynamic shared memory per CTA. */
+ * KV head) unit and dynamic shared memory per CTA.  Units go to the split-K
+ * kernel (2-8 CTAs per unit in one cluster) only when there are fewer units
+ * than persistent CTAs (two per SM) and every CTA of a cluster still streams
+ * at least 64 16-token blocks; otherwise each unit runs whole on the
+ * persistent kernel (splits = 1).  confkv_launch_plan does the same planning
+ * without a context. */
 int confkv_attention_plan(confkv_ctx* ctx, int32_t* splits, int32_t* smem_bytes);
 
 /* Caps the attention grid at `ctas` CTAs; 0 (the default) lets the

@@ -49,3 +49,21 @@ def test_reference_arm_does_no_work_off_rank_zero(monkeypatch, capsys):
     monkeypatch.setenv("WORLD_SIZE", "2")
     assert bench.main(["--impl", "reference", "--steps", "3", "--warmup", "3"]) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_line_on_rank_zero(monkeypatch, capsys):
+    # the float64 oracle timed on the host: one JSON line with the same
+    # metric and unit as the GPU arm, its own cpu_baseline and a host-only e2e
+    import json
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    assert bench.main(["--impl", "reference", "--workload", "gpt2_b1", "--steps", "2",
+                       "--warmup", "3"]) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["unit"] == "steps/s" and line["higher_is_better"] is True
+    assert line["value"] > 0 and line["steps"] == 2 and line["warmup"] >= 3
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "steps/s",
+                           "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert line["config"]["workload"] == "gpt2_b1"

@@ -23,7 +23,9 @@ from _parity import OUT_TOL, TAU_BAND, check_evictions, compare_unit, unit_to_ho
 pytestmark = pytest.mark.gpu
 
 
-def _sampled_fullsize(name, seed, steps, n_units, expect_splits=None):
+def _sampled_fullsize(name, seed, steps, n_units, expect_splits=None, pool=0, extra_units=()):
+    # pool > 0: the step inputs are `pool` draws reused round-robin (as in
+    # the benchmark), so a long run needs no more than `pool` input sets
     w = get_workload(name)
     prm = orc.Params.from_workload(w)
     k, v = prefill_batch(w, seed, "cpu")
@@ -34,15 +36,19 @@ def _sampled_fullsize(name, seed, steps, n_units, expect_splits=None):
     if expect_splits is not None:
         assert expect_splits(splits), "launch shape %d CTAs per unit" % splits
     rng = np.random.default_rng(seed)
-    units = sorted({(int(rng.integers(w.B)), int(rng.integers(w.L))) for _ in range(n_units)})
+    units = sorted({(int(rng.integers(w.B)), int(rng.integers(w.L))) for _ in range(n_units)}
+                   | set(extra_units))
     states = {}
     for b, l in units:
         kk, vv = prefill_unit(w, seed, b, l)
         states[(b, l)] = orc.prefill_unit(kk, vv, w.W)
-    q, kn, vn, lg = step_pool(w, seed, steps, "cpu")
+    R = pool or steps
+    q, kn, vn, lg = step_pool(w, seed, R, "cpu")
     flagged = 0
+    flips = 0
     for s in range(steps):
-        o = cache.step(q[s].cuda(), kn[s].cuda(), vn[s].cuda(), lg[s].cuda())
+        j = s % R
+        o = cache.step(q[j].cuda(), kn[j].cuda(), vn[j].cuda(), lg[j].cuda())
         torch.cuda.synchronize()
         out = o["out"].cpu().numpy()
         bud = o["budget"].cpu().numpy()
@@ -50,9 +56,10 @@ def _sampled_fullsize(name, seed, steps, n_units, expect_splits=None):
         ev = o["evicted"].cpu().numpy()
         t = w.T0 + s
         for b, l in units:
-            c = orc.confidence(step_logits(w, seed, s, b)).c
+            c = orc.confidence(step_logits(w, seed, j, b)).c
             N = orc.budget(c, w.tau, w.n_high[l], w.n_low[l])
-            qq, kk, vv = step_unit(w, seed, s, b, l)
+            flips += N == w.n_high[l]
+            qq, kk, vv = step_unit(w, seed, j, b, l)
             r = orc.step_unit(prm, states[(b, l)], t, qq.float().numpy(), kk, vv, N)
             states[(b, l)] = r.state
             where = "%s step %d b%d l%d" % (name, s, b, l)
@@ -71,7 +78,7 @@ def _sampled_fullsize(name, seed, steps, n_units, expect_splits=None):
     for b, l in units:
         compare_unit(cache.export_unit(b, l), states[(b, l)], "%s final b%d l%d" % (name, b, l))
     assert cache.stats()["device_status"] == 0
-    return flagged
+    return flagged, flips
 
 
 def test_qwen32b_shape_sampled_units():
@@ -80,7 +87,12 @@ def test_qwen32b_shape_sampled_units():
 
 
 def test_qwen14b_shape_sampled_units():
-    _sampled_fullsize("qwen14b", 4002, steps=3, n_units=4, expect_splits=lambda sp: sp == 1)
+    # 40 steps from a pool of 16 input draws: sequence 0 takes the tight
+    # budget at the first step (8192 -> 1024 entries) and again at steps 6,
+    # 16, 22, 32 and 38, sequence 3 at steps 8, 12, 24 and 28
+    _, flips = _sampled_fullsize("qwen14b", 4002, steps=40, n_units=4, expect_splits=lambda sp: sp == 1,
+                                 pool=16, extra_units=[(0, 5), (3, 47)])
+    assert flips >= 8
 
 
 def test_needle32k_first_steps():

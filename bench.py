@@ -55,29 +55,109 @@ def _peaks():
 
 
 def _traffic_ratio_from_profiles(kernel_tag: str):
-    """DRAM bytes per algorithmic byte of a kernel, from the committed ncu
-    summary line `dram_bytes_per_algorithmic_byte: <float>` of
-    profiles/<kernel_tag>.md, if present.  Each unit streams its own K/V
-    once, so traffic grows in proportion to the algorithmic bytes and a
-    launch's traffic is this ratio times its algorithmic bytes."""
-    p = os.path.join(ROOT, "profiles", kernel_tag + ".md")
+    """DRAM bytes per algorithmic byte of a kernel, from the machine-readable
+    ncu record profiles/<kernel_tag>.json (key
+    `dram_bytes_per_algorithmic_byte`), or None if there is none or it does
+    not describe the kernel now built (`stale`: true).  Each unit streams its
+    own K/V once, so traffic grows in proportion to the algorithmic bytes and
+    a launch's traffic is this ratio times its algorithmic bytes."""
+    p = os.path.join(ROOT, "profiles", kernel_tag + ".json")
     if not os.path.exists(p):
         return None
-    for line in open(p):
-        if line.strip().startswith("dram_bytes_per_algorithmic_byte:"):
-            try:
-                return float(line.split(":", 1)[1].strip().split()[0])
-            except ValueError:
-                return None
-    return None
+    try:
+        rec = json.load(open(p))
+    except (OSError, ValueError):
+        return None
+    if rec.get("stale"):
+        return None
+    r = rec.get("dram_bytes_per_algorithmic_byte")
+    return float(r) if isinstance(r, (int, float)) else None
+
+
+def blas_threads() -> dict:
+    """Threads the BLAS behind numpy may use: threadpoolctl where installed,
+    else the thread count reported by the OpenBLAS library numpy has loaded
+    (its exported get_num_threads call), else the environment."""
+    try:
+        from threadpoolctl import threadpool_info
+        info = [x for x in threadpool_info() if x.get("user_api") == "blas"]
+        if info:
+            return {"threads": max(int(x["num_threads"]) for x in info),
+                    "library": str(info[0].get("internal_api")), "how": "threadpoolctl"}
+    except Exception:
+        pass
+    try:
+        import ctypes
+        import numpy  # noqa: F401  (loads its BLAS)
+        libs = sorted({ln.split()[-1] for ln in open("/proc/self/maps") if "openblas" in ln.lower()})
+        for path in libs:
+            lib = ctypes.CDLL(path)
+            for name in ("scipy_openblas_get_num_threads64_", "openblas_get_num_threads64_",
+                         "scipy_openblas_get_num_threads", "openblas_get_num_threads"):
+                f = getattr(lib, name, None)
+                if f is not None:
+                    f.restype = ctypes.c_int
+                    return {"threads": int(f()), "library": os.path.basename(path), "how": name}
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return {"threads": int(os.environ[var]), "library": None, "how": var}
+    return {"threads": None, "library": None, "how": "unknown"}
+
+
+def untimed_steps(warmup: int, pool: int) -> int:
+    """Decode steps run before the timed window: at least the W warm-up
+    steps, and at least the first step (which cuts the prefill down to the
+    budget) plus one full cycle of the R-entry step-input pool.  The cache
+    length then follows its periodic regime, in which the pool's confident
+    entries flip the budget at fixed points of every cycle, so a short timed
+    window sees the same cache sizes as a long one."""
+    return max(int(warmup), int(pool) + 1)
+
+
+def spin_cycles(steps: int, clock_ghz: float = 2.07) -> int:
+    """GPU clock cycles of the device delay queued before the first timed
+    event: long enough for the host to queue the window's first steps behind
+    it (about 60 us of host time per step, at most 50 ms), so that neither
+    the host's launch latency nor an idle GPU's clock ramp falls inside the
+    timed window."""
+    ms = min(50.0, 2.0 + 0.06 * max(int(steps), 1))
+    return int(ms * 1e-3 * clock_ghz * 1e9)
+
+
+def l2_note(w) -> str:
+    """How the timed window relates to the 129 MB L2, from the workload's
+    steady-state K/V bytes per step (each cache at its loose budget)."""
+    n = min(max(w.n_low), w.T0 + w.steps)
+    n8 = max(0, n - w.W)
+    nr = min(n, w.W + 16)
+    kv = w.L * w.B * w.Hkv * w.d * (2 * n8 + 4 * nr)
+    if kv > 129e6:
+        return "inputs larger than L2: ~%.2f GB of K/V streamed per step > 129 MB L2, no flush" % (kv / 1e9)
+    return ("K/V of ~%.1f MB per step fits the 129 MB L2 and stays resident between steps "
+            "(not flushed)" % (kv / 1e6))
+
+
+def bench_config(w, args, ws: int) -> dict:
+    """The `config` object of the JSON line: the same dict for both arms."""
+    return {"workload": w.name, "compaction": args.compaction, "global_batch": w.B * ws,
+            "seq_len": w.T0, "layers": w.L, "heads": [w.Hq, w.Hkv], "head_dim": w.d, "vocab": w.V,
+            "budgets": [w.n_high[0], w.n_low[0]], "budgets_last_layer": [w.n_high[-1], w.n_low[-1]],
+            "P": w.P, "W": w.W, "query_dtype": w.q_dtype,
+            "parallelism": "replicas (dp%d over sequences)" % ws, "l2": l2_note(w)}
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    """nvidia-smi clocks, utilisation and throttle reasons sampled every
+    200 ms.  `stop` reports the median SM clock over the samples taken under
+    load (GPU utilisation >= 50 %; all samples if none was), and every
+    throttle reason seen while sampling."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,"
+              "utilization.gpu")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -106,17 +186,31 @@ class ClockSampler:
         rows = []
         for line in open(self.path):
             f = [x.strip() for x in line.split(",")]
-            if len(f) >= 9:
+            if len(f) >= 10:
                 rows.append(f)
         os.unlink(self.path)
-        if not rows:
-            return None
-        sm = sorted(float(r[1]) for r in rows if r[1].replace(".", "").isdigit())
-        mx = max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit())
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
-        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx, "reasons": reasons,
-                "samples": len(rows)}
+        return summarise_clocks(rows)
+
+
+def _num(x):
+    try:
+        return float(x)
+    except ValueError:
+        return None
+
+
+def summarise_clocks(rows):
+    """Summary of nvidia-smi rows in ClockSampler.FIELDS order."""
+    if not rows:
+        return None
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    loaded = [r for r in rows if (_num(r[9]) or 0.0) >= 50.0]
+    use = loaded or rows
+    sm = sorted(v for v in (_num(r[1]) for r in use) if v is not None)
+    mx = [v for v in (_num(r[2]) for r in rows) if v is not None]
+    reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+    return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": max(mx) if mx else None,
+            "reasons": reasons, "samples": len(rows), "samples_under_load": len(loaded)}
 
 
 def _dist():
@@ -178,6 +272,7 @@ def cpu_baseline(w, seed: int, units: int = 8, steps: int = 120):
         "unit": "steps/s",
         "cores": max(1, int(round(cpu / wall))) if wall > 0 else 1,
         "cores_available": len(os.sched_getaffinity(0)),
+        "blas": blas_threads(),
         "kind": "oracle",
         "sample": "%d (sequence, layer) unit-steps of %s at steady-state cache size (confidence "
                   "over the full vocabulary, attention, EMA, ranking, eviction, requantisation), "
@@ -186,12 +281,20 @@ def cpu_baseline(w, seed: int, units: int = 8, steps: int = 120):
 
 
 def run_reference(args):
+    """The reference arm: the float64 oracle timed on the host cores, on the
+    GPU arm's workload and config.  Each timed step runs a bounded sample of
+    the workload (2 (sequence, layer) unit-steps at steady-state cache size);
+    `value` extrapolates it to whole steps (all L x B units), `ms_per_step` is
+    the measured wall time of one timed step."""
     from workload import get_workload
     ws, rank, _ = _dist()
     if rank != 0:
         return 0
     w = get_workload(args.workload)
-    smp = OracleSample(w, args.seed, units=2)
+    if args.batch:
+        w = w.replace(B=args.batch)
+    units = 2
+    smp = OracleSample(w, args.seed, units=units)
     for _ in range(args.warmup):
         smp.run(1)
     vals = []
@@ -206,20 +309,30 @@ def run_reference(args):
     v = vals[len(vals) // 2]
     cpu_line = {"value": v, "unit": "steps/s",
                 "cores": max(1, int(round(tot_cpu / tot_wall))) if tot_wall > 0 else 1,
-                "cores_available": len(os.sched_getaffinity(0)), "kind": "oracle",
-                "sample": "each step: 2 (sequence, layer) unit-steps of %s at steady-state size; "
-                          "steps/s = 1 / (time per unit-step x L x B), median over steps" % w.name}
+                "cores_available": len(os.sched_getaffinity(0)), "blas": blas_threads(), "kind": "oracle",
+                "sample": "each timed step: %d (sequence, layer) unit-steps of %s at steady-state size; "
+                          "steps/s = 1 / (time per unit-step x L x B), median over steps" % (units, w.name)}
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "steps/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / v,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * tot_wall / max(args.steps, 1),
+        "extrapolated": {"ms_per_whole_step": 1000.0 / v, "unit_steps_per_timed_step": units,
+                         "unit_steps_per_whole_step": w.L * w.B,
+                         "how": "value = whole-step rate extrapolated from the timed unit-steps; "
+                                "ms_per_step = measured wall time of one timed step"},
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": w.name, "global_batch": w.B, "seq_len": w.T0,
-                                         "layers": w.L, "parallelism": "replicas"},
+        "data": "synthetic", "config": bench_config(w, args, ws),
         "cpu_baseline": cpu_line,
         "e2e": {"value": v, "unit": "steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
     return 0
+
+
+def replica_seed(base: int, i: int, rank: int) -> int:
+    """Seed of the i-th timed instance on `rank`: replicas on different ranks
+    draw different prefills and step inputs."""
+    return base + i + 7919 * rank
 
 
 def reduce_timing(ms: float, steps: int, world_size: int, device):
@@ -257,9 +370,13 @@ def run_ours(args):
     stream = torch.cuda.current_stream()
     every = profile_stride(R)
 
+    pre = untimed_steps(args.warmup, R)
+    clocks = ClockSampler(local)
+    clocks.start()
+
     def timed_seed(seed):
-        """Prefill, W warm-up steps, then exactly K timed steps of one seeded
-        instance of the workload."""
+        """Prefill, the untimed steps (at least W warm-up steps), then exactly
+        K timed steps of one seeded instance of the workload."""
         cache = ck.Cache(cfg, device=dev)
         k, v = prefill_batch_fast(w, seed, dev)
         cache.prefill(k, v, [w.T0] * w.B)
@@ -269,13 +386,10 @@ def run_ours(args):
         pool = step_pool_fast(w, seed, R, dev)
         q, kn, vn, lg = pool
         outs = cache.new_outputs()
-        for s in range(args.warmup):
+        for s in range(pre):
             cache.step(q[s % R], kn[s % R], vn[s % R], lg[s % R], outs)
         torch.cuda.synchronize()
         st0 = cache.stats()
-        clocks = ClockSampler(local)
-        clocks.start()
-        time.sleep(0.3)
         # per-kernel events on every `every`-th timed step: an event record
         # between kernels costs the stream ~2 us, so recording all four on
         # every step would slow the very steps it times
@@ -284,21 +398,24 @@ def run_ours(args):
             dist.barrier()
         torch.cuda.synchronize()
         ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # a device delay ahead of the first event: the host queues the
+        # window's first steps behind it, so the window measures the GPU
+        # running the steps back to back, not the host's first launches
+        torch.cuda._sleep(spin_cycles(args.steps))
         ev0.record(stream)
         for s in range(args.steps):
-            j = (args.warmup + s) % R
+            j = (pre + s) % R
             cache.step(q[j], kn[j], vn[j], lg[j], outs)
         ev1.record(stream)
         torch.cuda.synchronize()
         if ws > 1:
             dist.barrier()
         ms = ev0.elapsed_time(ev1)
-        clk = clocks.stop()
         prof = cache.profile_read()
         cache.profile_disable()
         st1 = cache.stats()
         ms_max, sps = reduce_timing(ms, args.steps, ws, dev)
-        return dict(seed=seed, cache=cache, pool=pool, outs=outs, st0=st0, st1=st1, prof=prof, clk=clk,
+        return dict(seed=seed, cache=cache, pool=pool, outs=outs, st0=st0, st1=st1, prof=prof,
                     ms_max=ms_max, sps=sps)
 
     # The pages report the median of three seeds: each seed is its own
@@ -306,21 +423,17 @@ def run_ours(args):
     # rate and every per-kernel figure come from the median seed.
     runs = []
     for i in range(max(1, args.seeds)):
-        r = timed_seed(args.seed + i + 7919 * rank)
+        r = timed_seed(replica_seed(args.seed, i, rank))
         if runs:   # only the last seed's cache stays for the e2e and graph runs
             for key in ("cache", "pool", "outs"):
                 runs[-1].pop(key, None)
             torch.cuda.empty_cache()
         runs.append(r)
+    clk = clocks.stop()
     med = sorted(runs, key=lambda r: r["sps"])[len(runs) // 2]
     cache, outs = runs[-1]["cache"], runs[-1]["outs"]
     q, kn, vn, lg = runs[-1]["pool"]
     st0, st1, prof, ms_max, steps_per_s = med["st0"], med["st1"], med["prof"], med["ms_max"], med["sps"]
-    clk = med["clk"]
-    if clk is not None:
-        clk = dict(clk)
-        clk["reasons"] = sorted({x for r in runs if r["clk"] for x in r["clk"]["reasons"]})
-        clk["samples"] = sum(r["clk"]["samples"] for r in runs if r["clk"])
     seeds = {"values": [r["sps"] for r in runs], "seeds": [r["seed"] for r in runs],
              "reported": "median" if len(runs) > 1 else "single"}
 
@@ -376,10 +489,11 @@ def run_ours(args):
         graphs = [cache.capture_step(q[j], kn[j], vn[j], lg[j], outs) for j in range(R)]
         torch.cuda.synchronize()
         g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(spin_cycles(args.steps))
         g0.record(stream)
         done = 0
         for s in range(args.steps):
-            graphs[(args.warmup + s) % R].replay()
+            graphs[(pre + s) % R].replay()
             if (s + 1) % 64 == 0:
                 cache.graph_advance(s + 1 - done)
                 done = s + 1
@@ -414,12 +528,13 @@ def run_ours(args):
             "vs_baseline": None,
             "dtype": "fp16/int8 storage, fp16 tensor-core products, fp32 accumulate",
             "data": "synthetic",
-            "config": {"workload": w.name, "compaction": args.compaction, "global_batch": w.B * ws,
-                       "seq_len": w.T0, "layers": w.L,
-                       "heads": [w.Hq, w.Hkv], "head_dim": w.d, "vocab": w.V,
-                       "budgets": [w.n_high[0], w.n_low[0]], "P": w.P, "W": w.W,
-                       "parallelism": "replicas (dp%d over sequences)" % ws,
-                       "l2": "per-step K/V stream %.2f GB > 129 MB L2, no flush" % (step_bytes / 1e9)},
+            "config": bench_config(w, args, ws),
+            "untimed_steps": {"count": pre, "warmup": args.warmup,
+                              "why": "at least W warm-up steps, and at least the first step plus one "
+                                     "cycle of the %d-entry step-input pool, so the timed window starts "
+                                     "in the cache's periodic regime" % R},
+            "timed_window": "CUDA events on the launching stream around exactly K steps, queued behind "
+                            "a device delay so that host launch latency stays outside the window",
             "hbm": {"achieved_gbs": step_bytes / (ms_max / args.steps / 1000.0) / 1e9,
                     "algorithmic_bytes_per_step": step_bytes, "peak_gbs": peak, "peak_kind": peak_kind,
                     "frac": step_bytes / (ms_max / args.steps / 1000.0) / 1e9 / peak},
@@ -433,7 +548,7 @@ def run_ours(args):
             "kernel_timing": "CUDA events around each kernel on every %dth timed step (%d steps sampled)"
                              % (every, prof["steps"]),
             "attention_launch": {"ctas_per_unit": splits, "smem_bytes": smem},
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": int(st1["launches"] - st0["launches"]),
             "clocks": clk,
             "e2e": e2e,
             "graph": graph,
@@ -474,6 +589,13 @@ def variant_workload(w, kind: str, steps_total: int):
     raise ValueError(kind)
 
 
+def prefill_kv_bytes(w, T0: int) -> int:
+    """K/V bytes at stored widths right after a prefill of T0 tokens per
+    sequence: positions older than the W newest in INT8, the rest in FP16."""
+    n8 = max(0, T0 - w.W)
+    return w.L * w.B * w.Hkv * w.d * (2 * n8 + 4 * (T0 - n8))
+
+
 def run_compare(args):
     """One JSON line: per-step latency (CUDA events around every step), the
     step rate and the peak resident KV bytes of each policy over the same
@@ -507,20 +629,23 @@ def run_compare(args):
             cache.step(q[s % R], kn[s % R], vn[s % R], lg[s % R], outs)
         torch.cuda.synchronize()
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(gen)]
-        peak = cache.stats()["resident_bytes"]
         for s in range(gen):
             j = (args.warmup + s) % R
             evs[s][0].record(stream)
             cache.step(q[j], kn[j], vn[j], lg[j], outs)
             evs[s][1].record(stream)
-            if (s + 1) % 256 == 0 or s == gen - 1:
-                peak = max(peak, cache.stats()["resident_bytes"])   # synchronises
         torch.cuda.synchronize()
         ms = np.array([a.elapsed_time(b) for a, b in evs])
         st = cache.stats()
+        # peak K/V bytes at stored widths: the exact maximum over the ends of
+        # all steps since prefill, kept on the device; the workspace is the
+        # allocator footprint (all device memory the context holds)
         res[kind] = {"p50_ms": float(np.median(ms)), "mean_ms": float(ms.mean()),
                      "p90_ms": float(np.percentile(ms, 90)), "steps_per_s": 1000.0 / float(ms.mean()),
-                     "peak_kv_bytes": int(peak), "final_resident_entries": int(st["resident"]),
+                     "peak_kv_bytes": int(st["peak_resident_bytes"]), "peak_entries": int(st["peak_resident"]),
+                     "prefill_kv_bytes": int(prefill_kv_bytes(w, w0.T0)),
+                     "workspace_bytes": int(st["workspace_bytes"]),
+                     "final_resident_entries": int(st["resident"]),
                      "W": w.W, "budgets": [w.n_high[0], w.n_low[0]], "alpha": w.alpha}
         del cache, outs
         torch.cuda.empty_cache()
@@ -532,7 +657,8 @@ def run_compare(args):
             "ratios": {"p50_latency_fullkv_over_confkv": f["p50_ms"] / c["p50_ms"],
                        "throughput_confkv_over_fullkv": f["mean_ms"] / c["mean_ms"],
                        "throughput_sliding512_over_fullkv": f["mean_ms"] / sl["mean_ms"],
-                       "peak_kv_fullkv_over_confkv": f["peak_kv_bytes"] / max(c["peak_kv_bytes"], 1)},
+                       "peak_kv_fullkv_over_confkv": f["peak_kv_bytes"] / max(c["peak_kv_bytes"], 1),
+                       "workspace_fullkv_over_confkv": f["workspace_bytes"] / max(c["workspace_bytes"], 1)},
             "pages": {"p50_latency_fullkv_over_confkv": 1.8, "throughput_confkv_over_fullkv_batch8": 2.06,
                       "note": "GPT-2 / Qwen-32B at 2048 generated tokens on the pages' GPU; context only"}}
     print(json.dumps(line), flush=True)

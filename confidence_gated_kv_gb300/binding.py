@@ -60,6 +60,8 @@ class Stats(ctypes.Structure):
         ("step_bytes", ctypes.c_double), ("resident", ctypes.c_int64),
         ("resident_bytes", ctypes.c_int64), ("device_status", ctypes.c_int32),
         ("host_h2d_bytes", ctypes.c_int64), ("host_d2h_bytes", ctypes.c_int64),
+        ("peak_resident", ctypes.c_int64), ("peak_resident_bytes", ctypes.c_int64),
+        ("workspace_bytes", ctypes.c_int64), ("launches", ctypes.c_int64),
     ]
 
 

@@ -149,6 +149,7 @@ struct confkv_ctx {
   long long n8_bound = 0;   // max INT8 entries of any (l, b)
   int minN = 0, maxN = 0;
   long long host_h2d = 0, host_d2h = 0;   // bytes of the last confkv_step_host
+  long long launches = 0;                  // kernels launched by decode steps
   // confkv_step_host: a second stream copies the attention output back while
   // the select kernel runs (created on first use)
   cudaStream_t aux = nullptr;
@@ -165,6 +166,18 @@ struct confkv_ctx {
 };
 
 static int cuda_status(cudaError_t e) { return e == cudaSuccess ? CONFKV_OK : CONFKV_ECUDA; }
+static bool aligned(const void* p, uintptr_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
+
+// Alignment the decode kernels rely on: q is read with bulk copies (16-byte
+// source addresses), k_new / v_new as 32-bit words, every other buffer as
+// 4-byte elements.
+static bool step_args_aligned(const void* q, const void* k_new, const void* v_new, const float* logits,
+                              const float* out, const int32_t* budget, const float* confidence,
+                              const int32_t* evicted_pos, const int32_t* n_evicted) {
+  return aligned(q, 16) && aligned(k_new, 4) && aligned(v_new, 4) && aligned(logits, 4) && aligned(out, 4) &&
+         aligned(budget, 4) && (!confidence || aligned(confidence, 4)) && aligned(evicted_pos, 4) &&
+         aligned(n_evicted, 4);
+}
 static cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
 extern "C" {
@@ -237,6 +250,7 @@ int confkv_prefill(confkv_ctx* ctx, const int32_t* prefill_len, const void* k, c
     tmax0 = std::max<long long>(tmax0, prefill_len[b]);
   }
   if (tmax0 > 0 && (!k || !v)) return CONFKV_EINVAL;
+  if (tmax0 > 0 && (!aligned(k, 2) || !aligned(v, 2))) return CONFKV_EINVAL;
   if (tmax0 - s.W > s.cap) return CONFKV_ECAPACITY;
   cudaStream_t st = as_stream(stream);
   ctx->T0.assign(prefill_len, prefill_len + s.B);
@@ -399,6 +413,8 @@ static int step_impl(confkv_ctx* ctx, const void* q, const void* k_new, const vo
   if (!ctx->prefilled) return CONFKV_ESTATE;
   if (!q || !k_new || !v_new || !logits || !out || !budget || !evicted_pos || !n_evicted)
     return CONFKV_EINVAL;
+  if (!step_args_aligned(q, k_new, v_new, logits, out, budget, confidence, evicted_pos, n_evicted))
+    return CONFKV_EINVAL;
   const Shape& s = ctx->s;
   cudaStream_t st = as_stream(stream);
   // Under stream capture nothing runs now: the launches go into a graph
@@ -432,6 +448,7 @@ static int step_impl(confkv_ctx* ctx, const void* q, const void* k_new, const vo
   if (prof) cudaEventRecord(ev[2], st);
   if (after_attention && cudaEventRecord(after_attention, st) != cudaSuccess) return CONFKV_ECUDA;
   if (launch_select(s, ctx->d, step_arg, evicted_pos, n_evicted, st) != 0) return CONFKV_ECUDA;
+  if (!capturing) ctx->launches += 3;
   if (prof) {
     cudaEventRecord(ev[3], st);
     ctx->prof_count++;
@@ -542,7 +559,11 @@ int confkv_step_host(confkv_ctx* ctx, const void* q, const void* k_new, const vo
   const bool mapped = device_view(k_new, &mk) && device_view(v_new, &mv) && device_view(logits, &ml) &&
                       device_view(out, &mo) && device_view(budget, &mb) &&
                       (!confidence || device_view(confidence, &mc)) && device_view(evicted_pos, &me) &&
-                      device_view(n_evicted, &mn);
+                      device_view(n_evicted, &mn) &&
+                      step_args_aligned(ctx->st.q, mk, mv, static_cast<const float*>(ml),
+                                        static_cast<const float*>(mo), static_cast<const int32_t*>(mb),
+                                        confidence ? static_cast<const float*>(mc) : nullptr,
+                                        static_cast<const int32_t*>(me), static_cast<const int32_t*>(mn));
   if (mapped) {
     cudaError_t e = cudaEventRecord(ctx->ev_in, st);   // g.q is free once earlier work on `stream` is
     if (e == cudaSuccess) e = cudaStreamWaitEvent(ctx->aux, ctx->ev_in, 0);
@@ -793,6 +814,10 @@ int confkv_get_stats(confkv_ctx* ctx, confkv_stats* out, void* stream) {
   out->device_status = status;
   out->host_h2d_bytes = ctx->host_h2d;
   out->host_d2h_bytes = ctx->host_d2h;
+  out->peak_resident = (int64_t)ds.peak_entries;
+  out->peak_resident_bytes = (int64_t)ds.peak_bytes;
+  out->workspace_bytes = (int64_t)ctx->ws_bytes;
+  out->launches = ctx->launches;
   return status ? CONFKV_EDEVICE : CONFKV_OK;
 }
 

@@ -194,6 +194,8 @@ int scratch_on_current_device(Partial** out) {
 extern "C" int confkv_confidence_noalloc(const float* logits, int32_t B, int32_t V, double w_H,
                                          double w_m, double w_p, float* confidence, void* stream) {
   if (!logits || !confidence || B < 1 || V < 2) return CONFKV_EINVAL;
+  if (reinterpret_cast<uintptr_t>(logits) % 4 || reinterpret_cast<uintptr_t>(confidence) % 4)
+    return CONFKV_EINVAL;
   if (!std::isfinite(w_H) || !std::isfinite(w_m) || !std::isfinite(w_p)) return CONFKV_EINVAL;
   const long long parts = (V + (long long)kChunk - 1) / kChunk;
   if ((long long)B * parts > kMaxPartials) return CONFKV_ECAPACITY;

@@ -96,6 +96,12 @@ struct DevStats {        // cumulative counters, updated with atomics
   unsigned long long requant;
   unsigned long long attn_bytes;   // algorithmic bytes of the attention kernel
   unsigned long long step_bytes;   // algorithmic bytes of the whole step
+  // resident footprint after each step: every select CTA adds its (layer,
+  // sequence)'s entries and K/V bytes; the last CTA of the step takes the
+  // sums, keeps their maximum over steps and zeroes them for the next step
+  unsigned long long res_entries_acc, res_bytes_acc;
+  unsigned long long peak_entries, peak_bytes;
+  unsigned long long sel_arrivals;
 };
 
 struct Shape {

@@ -171,7 +171,6 @@ __global__ void __launch_bounds__(kConfThreads) prestep_kernel(Shape s, Dev d, l
                                                                const __half* __restrict__ v_new,
                                                                int nconf) {
   pdl_wait();
-  if (blockIdx.x == 0 && threadIdx.x == 0) atomicAdd(&d.stats->steps, 1ull);
   if ((int)blockIdx.x < nconf) {
     conf_block(s, d, logits, blockIdx.x / s.SV, blockIdx.x % s.SV);
   } else {

@@ -723,6 +723,22 @@ __global__ void __launch_bounds__(kSelThreads, 4) select_kernel(Shape s, Dev d, 
     atomicAdd(&d.stats->attn_bytes, attn);
     atomicAdd(&d.stats->step_bytes, step_b);
     if (blockIdx.x == 0) atomicAdd(&d.stats->steps, 1ull);
+    // resident footprint of this (layer, sequence) after the step: the INT8
+    // region and the ring entries that neither were evicted nor left for INT8
+    const unsigned long long ring_after = (unsigned long long)(nring - (cnt - k8) - requant);
+    atomicAdd(&d.stats->res_entries_acc, (unsigned long long)n8n + ring_after);
+    atomicAdd(&d.stats->res_bytes_acc, Hk * Dl * (2ull * (unsigned long long)n8n + 4ull * ring_after));
+    __threadfence();
+    if (atomicAdd(&d.stats->sel_arrivals, 1ull) == (unsigned long long)gridDim.x - 1ull) {
+      // last CTA of the step: every other CTA's sums are in
+      __threadfence();
+      const unsigned long long e = atomicExch(&d.stats->res_entries_acc, 0ull);
+      const unsigned long long by = atomicExch(&d.stats->res_bytes_acc, 0ull);
+      if (e > d.stats->peak_entries) d.stats->peak_entries = e;
+      if (by > d.stats->peak_bytes) d.stats->peak_bytes = by;
+      d.stats->sel_arrivals = 0ull;
+      __threadfence();
+    }
     if (kDevStep) {
       // the last CTA to finish advances the step index (every CTA has read it
       // before its own increment of the counter)

@@ -116,7 +116,8 @@ void confkv_destroy(confkv_ctx* ctx);
  * >= prefill_len - W stay FP16; older positions are stored as INT8 codes
  * clamp(rint(x / s), -127, 127) ([gist-de] Systemintegration; the pages do
  * not describe prefill, this rule follows their per-head per-channel INT8).
- * EMA mass starts at 0.  Returns CONFKV_ECAPACITY if prefill_len - W > cap.
+ * EMA mass starts at 0.  Returns CONFKV_ECAPACITY if prefill_len - W > cap,
+ * CONFKV_EINVAL if k or v is not 2-byte aligned.
  */
 int confkv_prefill(confkv_ctx* ctx, const int32_t* prefill_len, const void* k, const void* v,
                    int64_t t_max, void* stream);
@@ -144,6 +145,12 @@ int confkv_prefill(confkv_ctx* ctx, const int32_t* prefill_len, const void* k, c
  * evicts the n - N lowest s = alpha a_hat + (1 - alpha) r_hat among entries
  * older than the newest P, compacts the INT8 region, requantises the entry
  * that leaves the FP16 window and appends the new token.
+ * Alignment: q must be 16-byte aligned (the attention kernel copies query
+ * rows with bulk copies), k_new and v_new 4-byte aligned (read as 32-bit
+ * words), logits, out, budget, confidence, evicted_pos and n_evicted 4-byte
+ * aligned; otherwise CONFKV_EINVAL, before anything is launched.  Tensors
+ * from a torch allocation or a contiguous slice at a multiple of 8 elements
+ * satisfy all of these.
  * Returns CONFKV_ECAPACITY (before launching anything) if the worst case of
  * this step could overflow cap or max_evict.
  */
@@ -164,6 +171,9 @@ int confkv_step(confkv_ctx* ctx, const void* q, const void* k_new, const void* v
  *    workspace first, and the outputs are copied back (the attention output
  *    on the second stream while the last kernel runs).  Pinned memory makes
  *    these copies asynchronous DMA.
+ * Mapped mode also needs k_new and v_new 4-byte aligned and every other
+ * buffer but q 4-byte aligned; misaligned pinned buffers take the staged
+ * mode.  q has no alignment requirement here (it is always staged).
  * confidence may be NULL.  Of each row of evicted_pos only the first
  * n_evicted entries are meaningful; in mapped mode only those are written,
  * in staged mode as many as the step's worst-case eviction count are copied
@@ -261,6 +271,15 @@ typedef struct confkv_stats {
   int32_t device_status;     /* raw device status bits (0 = ok) */
   int64_t host_h2d_bytes;    /* bytes the last confkv_step_host moved host -> device */
   int64_t host_d2h_bytes;    /* bytes the last confkv_step_host moved device -> host */
+  int64_t peak_resident;     /* largest `resident` seen at the end of any step since
+                                prefill (exact: summed on the device every step) */
+  int64_t peak_resident_bytes; /* largest `resident_bytes` at the end of any step
+                                since prefill (the pages' peak KV memory, [rainbus]
+                                results table) */
+  int64_t workspace_bytes;   /* device bytes the context holds: the caller's
+                                workspace (the allocator footprint; fixed at create) */
+  int64_t launches;          /* kernels this context has launched for decode steps
+                                since it was created (host count) */
 } confkv_stats;
 
 /* Read the counters and the device status word (synchronises `stream`).
@@ -357,7 +376,8 @@ int32_t confkv_block_offset(int32_t kind, int32_t d, int32_t tau, int32_t c);
  * with that device current); make that first call before any stream capture.
  * Returns CONFKV_ECAPACITY, without launching anything, if
  * B * ceil(V / 4096) > CONFKV_NOALLOC_MAX_PARTIALS; CONFKV_EINVAL for null
- * pointers, B < 1, V < 2 or non-finite weights.  Asynchronous on `stream`.
+ * pointers, logits or confidence not 4-byte aligned, B < 1, V < 2 or
+ * non-finite weights.  Asynchronous on `stream`.
  */
 int confkv_confidence_noalloc(const float* logits, int32_t B, int32_t V, double w_H, double w_m,
                               double w_p, float* confidence, void* stream);

@@ -54,8 +54,10 @@ R6  INT8 scales per (sequence, layer, KV head, channel), K and V separately,
 R7  Prefill entries start with a = 0; a new token's EMA starts from 0, so
     after its first update a = (1 - lam) A_self.
 R8  Eviction order: (s ascending, position ascending).
-R9  The budget test is c >= tau, compared in float32 (the pages fix no
-    precision; the kernels form c in fp32), with c itself from float64 sums.
+R9  The budget test is c >= tau, exactly, in float64 (the pages fix no
+    precision).  A c within 1e-6 of tau may be decided the other way by an
+    implementation that forms c in fp32; the parity harness flags such steps
+    and checks the result against this rule applied with the other budget.
 R10 A duplicated maximum gives p(2) = p(1), m = 0.
 R12 Raw logits (temperature 1), natural logarithm.
 R13 Evicted entries are reported as absolute positions, ascending.
@@ -154,8 +156,8 @@ def confidence(logits, w_H=0.4, w_m=0.3, w_p=0.3) -> Confidence:
 def budget(c: float, tau: float, n_high: int, n_low: int) -> int:
     """N = N_high if c >= tau else N_low ([gist-de] Adaptive Budgetauswahl;
     [rainbus] Algorithm 1 step 4).  N_high is the tight budget.  The
-    comparison runs in float32 (R9)."""
-    return int(n_high) if np.float32(c) >= np.float32(tau) else int(n_low)
+    comparison is exact, in float64 (R9)."""
+    return int(n_high) if float(c) >= float(tau) else int(n_low)
 
 
 # ----------------------------------------------------------------------------

@@ -7,9 +7,12 @@ sampled unit.  Units evolve independently given their sequence's confidence,
 so a sample checks the same arithmetic as the full batch.
 
 An eviction decided by a near-tie (oracle scores within 1e-5 of the cut) or a
-budget with |c - tau| < 1e-6 may legitimately differ; the unit is then checked
-for validity and the GPU copy of that unit is replaced by the oracle's state
-(inputs only ever flow from the oracle to the GPU)."""
+budget with |c - tau| < 1e-6 may legitimately differ.  A budget that differs
+is checked by applying the oracle's eviction rule with the GPU's budget to
+the unit's pre-step state (same count, same set up to the tie band); a
+near-tie the same way with the oracle's own budget.  The GPU copy of that
+unit is then replaced by the oracle's state (inputs only ever flow from the
+oracle to the GPU)."""
 import numpy as np
 import pytest
 import torch
@@ -18,7 +21,7 @@ import confidence_gated_kv_gb300 as ck
 from oracle import confkv_oracle as orc
 from workload import get_workload, prefill_batch, prefill_unit, step_logits, step_pool, step_unit
 
-from _parity import OUT_TOL, TAU_BAND, check_evictions, compare_unit, unit_to_host
+from _parity import OUT_TOL, TAU_BAND, check_evictions, compare_unit, oracle_selection, unit_to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -60,18 +63,22 @@ def _sampled_fullsize(name, seed, steps, n_units, expect_splits=None, pool=0, ex
             N = orc.budget(c, w.tau, w.n_high[l], w.n_low[l])
             flips += N == w.n_high[l]
             qq, kk, vv = step_unit(w, seed, j, b, l)
-            r = orc.step_unit(prm, states[(b, l)], t, qq.float().numpy(), kk, vv, N)
+            pre = states[(b, l)]
+            r = orc.step_unit(prm, pre, t, qq.float().numpy(), kk, vv, N)
             states[(b, l)] = r.state
             where = "%s step %d b%d l%d" % (name, s, b, l)
             err = float(np.abs(out[l, b] - r.o).max())
             assert err <= OUT_TOL, "%s: attention error %.3g" % (where, err)
             same = bud[b, l] == N
+            sel = r
             if not same:
+                # the GPU took the other budget inside the tau band: its
+                # evictions must follow the rule with that budget
                 assert abs(c - w.tau) < TAU_BAND, where + ": budget differs"
-            else:
-                assert nev[l, b] == r.k, "%s: evicted %d vs %d" % (where, nev[l, b], r.k)
-                if r.k:
-                    same = check_evictions(ev[l, b, :r.k], r, where)
+                sel = oracle_selection(pre, r.a_updated, t, prm, int(bud[b, l]))
+            assert nev[l, b] == sel.k, "%s: evicted %d vs %d" % (where, nev[l, b], sel.k)
+            if sel.k and not check_evictions(ev[l, b, :sel.k], sel, where):
+                same = False
             if not same:
                 flagged += 1
                 cache.import_unit(b, l, unit_to_host(r.state))

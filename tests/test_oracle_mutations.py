@@ -29,7 +29,7 @@ def _run_pins():
         "range": pins.test_confidence_range_extremes,
         "constants": pins.test_weights_and_hyperparameters_match_pages,
         "tau_inclusive": pins.test_budget_threshold_is_inclusive,
-        "tau_f32": pins.test_budget_compares_in_float32,
+        "tau_f64": pins.test_budget_decides_in_float64,
         "sdpa": lambda: [pins.test_attention_matches_torch_sdpa(*a) for a in ((4, 4, 9), (10, 2, 37))],
         "online": lambda: [pins.test_online_softmax_equals_two_pass(b) for b in (1, 16, 1000)],
         "mass": pins.test_mass_is_head_average,
@@ -135,9 +135,11 @@ SLIPS = {
     "c: p(1) taken from the second token": ("confidence", _conf_variant("p1_second")),
     "c: entropy and margin weights swapped": ("confidence", _conf_variant("weights_swapped")),
     "budget: c > tau instead of c >= tau": (
-        "budget", lambda c, tau, nh, nl: int(nh) if np.float32(c) > np.float32(tau) else int(nl)),
+        "budget", lambda c, tau, nh, nl: int(nh) if float(c) > float(tau) else int(nl)),
     "budget: tight and loose swapped": (
-        "budget", lambda c, tau, nh, nl: int(nl) if np.float32(c) >= np.float32(tau) else int(nh)),
+        "budget", lambda c, tau, nh, nl: int(nl) if float(c) >= float(tau) else int(nh)),
+    "budget: compared in float32": (
+        "budget", lambda c, tau, nh, nl: int(nh) if np.float32(c) >= np.float32(tau) else int(nl)),
     # attention and mass
     "attention: no 1/sqrt(d)": ("attention", _attention_variant("no_sqrt_d")),
     "attention: KV head h % Hkv instead of h // G": ("attention", _attention_variant("kv_head_index")),

@@ -102,16 +102,21 @@ def test_weights_and_hyperparameters_match_pages():
 
 
 def test_budget_threshold_is_inclusive():
+    # [gist-de] Adaptive Budgetauswahl: c >= tau takes the tight budget; R9:
+    # exactly at tau counts, the next float64 below does not
     assert orc.budget(0.7, 0.7, 10, 20) == 10
-    below = float(np.nextafter(np.float32(0.7), np.float32(0)))
+    below = float(np.nextafter(0.7, 0.0))
     assert orc.budget(below, 0.7, 10, 20) == 20
-    above = float(np.nextafter(np.float32(0.7), np.float32(1)))
+    above = float(np.nextafter(0.7, 1.0))
     assert orc.budget(above, 0.7, 10, 20) == 10
 
 
-def test_budget_compares_in_float32():
-    # R9: a float64 c that rounds to float32(tau) counts as c >= tau
-    assert orc.budget(float(np.nextafter(0.7, 0)), 0.7, 10, 20) == 10
+def test_budget_decides_in_float64():
+    # R9 fixes no narrower precision: a c one float64 step below tau that
+    # would round up to float32(tau) still takes the loose budget
+    c = float(np.nextafter(0.7, 0.0))
+    assert np.float32(c) == np.float32(0.7)
+    assert orc.budget(c, 0.7, 10, 20) == 20
     assert orc.budget(0.5, 0.7, 10, 20) == 20 and orc.budget(0.9, 0.7, 10, 20) == 10
 
 

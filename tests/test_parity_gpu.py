@@ -355,3 +355,62 @@ def test_step_before_prefill_is_an_order_error():
     with pytest.raises(ck.ConfkvError) as e:
         c.step(*(t.cuda() for t in step_inputs(w, 19, 0)))
     assert e.value.status == -7
+
+
+def test_misaligned_buffers_are_refused_before_any_launch():
+    # q is read with bulk copies (16-byte aligned sources), k_new / v_new as
+    # 32-bit words: a view at an odd offset must come back as EINVAL with
+    # nothing launched, and the context must still step correctly after
+    import ctypes
+    w = Workload(name="t_align", B=2, L=2, Hq=8, Hkv=2, d=64, V=700, T0=60, steps=2,
+                 n_high=(24, 24), n_low=(40, 40), P=4, W=16, q_dtype="f16")
+    p = Pair(w, 25)
+    p.compare_states()
+    q, kn, vn, lg = (t.cuda() for t in step_inputs(w, 25, 0))
+    outs = p.cache.new_outputs()
+
+    def shifted(t, elems):
+        buf = torch.empty(t.numel() + 16, dtype=t.dtype, device="cuda")
+        v = buf[elems:elems + t.numel()].view(t.shape)
+        v.copy_(t)
+        return v
+
+    st0 = p.cache.stats()
+    L = ck.lib()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr())
+    cases = {"q +2 bytes": (shifted(q, 1), kn, vn, lg), "q +8 bytes": (shifted(q, 4), kn, vn, lg),
+             "k_new +2 bytes": (q, shifted(kn, 1), vn, lg), "v_new +2 bytes": (q, kn, shifted(vn, 1), lg)}
+    for name, (qq, kk, vv, ll) in cases.items():
+        r = L.confkv_step(p.cache.handle, ptr(qq), ptr(kk), ptr(vv), ptr(ll), ptr(outs["out"]),
+                          ptr(outs["budget"]), ptr(outs["confidence"]), ptr(outs["evicted"]),
+                          ptr(outs["n_evicted"]), stream)
+        assert r == ck.binding.EINVAL, "%s: status %d" % (name, r)
+    torch.cuda.synchronize()
+    st1 = p.cache.stats()
+    assert st1["launches"] == st0["launches"] and st1["steps"] == st0["steps"]
+    # a 16-byte-aligned view at an offset is fine
+    q8 = shifted(q, 8)
+    p.step(q.cpu(), kn.cpu(), vn.cpu(), lg.cpu(), gpu_step=lambda *a: p.cache.step(q8, kn, vn, lg))
+    assert p.cache.stats()["launches"] == st0["launches"] + 3
+    # the allocation-free confidence call checks its pointers the same way
+    c = torch.empty(w.B + 1, dtype=torch.float32, device="cuda")
+    lgs = shifted(lg, 1)
+    assert L.confkv_confidence_noalloc(ctypes.c_void_p(lgs.data_ptr() + 2), w.B, w.V, 0.4, 0.3, 0.3, ptr(c),
+                                       stream) == ck.binding.EINVAL
+    assert L.confkv_confidence_noalloc(ptr(lgs), w.B, w.V, 0.4, 0.3, 0.3,
+                                       ctypes.c_void_p(c.data_ptr() + 2), stream) == ck.binding.EINVAL
+
+
+def test_footprint_counters_follow_the_oracle():
+    # resident entries and K/V bytes at stored widths, and their exact peak
+    # over the steps, against the oracle's state (Pair checks every step);
+    # the workspace (allocator) bytes are the context's fixed footprint
+    w = Workload(name="t_foot", B=3, L=2, Hq=10, Hkv=2, d=128, V=3000, T0=300, steps=20,
+                 n_high=(40, 30), n_low=(120, 90), P=8, W=32, q_dtype="bf16")
+    p = _run(w, 26, 20, prefill_len=[300, 17, 0], confident_every=4)
+    st = p.cache.stats()
+    assert st["peak_resident"] == p.peak_entries > 0
+    assert st["peak_resident_bytes"] == p.peak_bytes > 0
+    assert st["workspace_bytes"] == ck.workspace_bytes(p.cache.cfg) == p.cache.workspace.numel()
+    assert st["steps"] == 20 and st["launches"] == 60

@@ -435,6 +435,8 @@ def run_ours(args):
     q, kn, vn, lg = runs[-1]["pool"]
     st0, st1, prof, ms_max, steps_per_s = med["st0"], med["st1"], med["prof"], med["ms_max"], med["sps"]
     seeds = {"values": [r["sps"] for r in runs], "seeds": [r["seed"] for r in runs],
+             "attention_ms": [r["prof"]["attention_ms"] / max(r["prof"]["steps"], 1) for r in runs],
+             "attention_bytes": [(r["st1"]["attn_bytes"] - r["st0"]["attn_bytes"]) / args.steps for r in runs],
              "reported": "median" if len(runs) > 1 else "single"}
 
     attn_bytes = (st1["attn_bytes"] - st0["attn_bytes"]) / args.steps

@@ -116,6 +116,13 @@ size_t layout(const Shape& s, char* base, Dev* d, Staging* st) {
   dd.scores = cv.take<float>((size_t)dd.score_ctas * 2 * s.G * s.S);
   dd.step_dev = cv.take<long long>(1);
   dd.sel_done = cv.take<uint32_t>(1);
+  dd.order = cv.take<int32_t>(lbs);
+  dd.queue = cv.take<uint32_t>(1);
+  // the persistent attention kernel takes its units longest first from a
+  // queue over prestep's sorted order (round robin when there are too many
+  // groups to sort in one prestep launch)
+  dd.sorted = lbs <= (size_t)kSortMaxGroups ? 1 : 0;
+  dd.sched = dd.sorted ? kSchedQueue : kSchedRoundRobin;
   Staging sg{};
   sg.q = cv.take<uint16_t>(lbs * s.Hq * s.D);
   sg.k_new = cv.take<uint16_t>(units * s.D);

@@ -764,6 +764,30 @@ struct RingPos {
   }
 };
 
+// Unit at position p of prestep's order (the (layer, sequence) groups with
+// the most INT8 entries first, the KV heads of a group in turn), or -1 past
+// the last unit.
+__device__ __forceinline__ int unit_of_rank(const Shape& s, const Dev& d, int units, int p) {
+  if (p >= units) return -1;
+  return __ldcg(d.order + p / s.Hkv) * s.Hkv + p % s.Hkv;
+}
+
+// k-th unit of this CTA, or -1 after its last (called by the producer only;
+// it hands each unit index to the other warps through shared memory).
+//   kSchedQueue       the next position of prestep's sorted order (longest
+//                     units first) from a counter that prestep zeroes every
+//                     step.  A CTA takes its next unit when it starts
+//                     streaming the current one, so the atomic stays off the
+//                     stream, and the CTAs that finish early take the
+//                     remaining units: the longest-first queue evens out the
+//                     CTAs' end times.
+//   kSchedRoundRobin  u = blockIdx.x + k * gridDim.x (groups not sorted).
+__device__ __forceinline__ int next_unit(const Shape& s, const Dev& d, int units, int k) {
+  if (d.sched == kSchedQueue) return unit_of_rank(s, d, units, (int)atomicAdd(d.queue, 1u));
+  const int u = (int)blockIdx.x + k * (int)gridDim.x;
+  return u < units ? u : -1;
+}
+
 template <int D, bool kFlush>
 __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
     Shape s, Dev d, const void* __restrict__ q, float* __restrict__ out,
@@ -779,7 +803,13 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
   float* wpart = reinterpret_cast<float*>(hbuf + 2 * hl.bytes);            // [2][4][G][D + 2]
   const int part_floats = kPConsumers * G * (D + 2);
   uint64_t* bars = reinterpret_cast<uint64_t*>(wpart + 2 * part_floats);
-  int& s_abort = *reinterpret_cast<int*>(bars + 2 * kPMaxStages + 8);
+  int* s_misc = reinterpret_cast<int*>(bars + 2 * kPMaxStages + 8);
+  int& s_abort = s_misc[0];
+  // unit index of header slot hs (set by the producer before its arrival on
+  // hfull) and of partials slot ps (set by consumer warp 0 before its arrival
+  // on done); -1 ends the CTA's work
+  volatile int* s_unit = s_misc + 1;    // [2]
+  volatile int* s_eunit = s_misc + 3;   // [2]
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
   auto empty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(kPMaxStages + i); };
@@ -824,14 +854,21 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
       const uint64_t pol = policy_evict_first();
       RingPos st;
       long long issued = 0;
-      int k = 0;
-      for (int u = blockIdx.x; u < units && !aborted(); u += gridDim.x, ++k) {
+      int u = next_unit(s, d, units, 0);
+      for (int k = 0; !aborted(); ++k) {
+        const int hs = k & 1;
+        if (k >= 2 && !mbar_wait(hempty_bar(hs), (uint32_t)(((k >> 1) - 1) & 1))) { fail(); break; }
+        if (u < 0) {
+          // no more units: the other warps see -1 in this header slot
+          s_unit[hs] = -1;
+          mbar_arrive(hfull_bar(hs));
+          break;
+        }
+        s_unit[hs] = u;
         const int h = u % s.Hkv, b = (u / s.Hkv) % s.B, l = u / (s.Hkv * s.B);
         const size_t lb = lb_index(s, l, b);
         const int nb8 = (d.n8[lb] + 15) >> 4;
         // unit header
-        const int hs = k & 1;
-        if (k >= 2 && !mbar_wait(hempty_bar(hs), (uint32_t)(((k >> 1) - 1) & 1))) { fail(); break; }
         const uint32_t hdst = smem_u32(hbuf + (size_t)hs * hl.bytes);
         const uint32_t qbytes = (uint32_t)(G * D * 2);
         mbar_arrive_tx(hfull_bar(hs), qbytes + 2u * D * 4 + (hl.pos_in ? (uint32_t)s.WR * 4 : 0u));
@@ -849,6 +886,7 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
         const char* k16u = reinterpret_cast<const char*>(d.k16) + (size_t)u * s.WR * D * 2;
         const char* v16u = reinterpret_cast<const char*>(d.v16) + (size_t)u * s.WR * D * 2;
         bool ok = true;
+        int u_next = -1;
         for (int i = 0; i < sch.nst; ++i) {
           if (issued >= stages && !mbar_wait(empty_bar(st.slot), st.phase ^ 1u)) { ok = false; break; }
           bool ring;
@@ -863,8 +901,11 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
           bulk_g2s_hint(dst + kHalf, vsrc, span, full_bar(st.slot), pol);
           st.next(stages);
           ++issued;
+          // the next unit is known early, so a queue's atomic stays off the stream
+          if (i == 0) u_next = next_unit(s, d, units, k + 1);
         }
         if (!ok) { fail(); break; }
+        u = sch.nst > 0 ? u_next : next_unit(s, d, units, k + 1);
       }
       // wait (bounded) for the last copy of every stage slot: nothing may be
       // in flight into shared memory when the CTA's threads have all exited
@@ -904,13 +945,14 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
       // the prestep kernel wrote the partials: merge the sequences this CTA owns
       for (int b = blockIdx.x; b < s.B; b += gridDim.x) conf_merge_warp(s, d, b, budget, conf_out);
     }
-    int k = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x, ++k) {
+    for (int k = 0;; ++k) {
       const int ps = k & 1;
       if (aborted() || !mbar_wait(done_bar(ps), (uint32_t)((k >> 1) & 1))) {
         if (!aborted()) fail();
         break;
       }
+      const int u = s_eunit[ps];
+      if (u < 0) break;
       const int h = u % s.Hkv, b = (u / s.Hkv) % s.B, l = u / (s.Hkv * s.B);
       const size_t lb = lb_index(s, l, b);
       const int nb8 = (d.n8[lb] + 15) >> 4;
@@ -986,15 +1028,22 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
   const float qs = kQPre * 1.4426950408889634f * rsqrtf((float)D);
   const uint64_t keep = policy_evict_last();
   RingPos st;
-  int k = 0;
-  for (int u = blockIdx.x; u < units; u += gridDim.x, ++k) {
+  for (int k = 0;; ++k) {
     const int hs = k & 1;
     if (aborted() || !mbar_wait(hfull_bar(hs), (uint32_t)((k >> 1) & 1))) {
       if (!aborted()) fail();
       break;
     }
+    const int u = s_unit[hs];
     if (k >= 2 && !mbar_wait(efree_bar(hs), (uint32_t)(((k >> 1) - 1) & 1))) {
       fail();
+      break;
+    }
+    // the epilogue takes the unit index with this unit's partials
+    if (warp == 0 && lane == 0) s_eunit[hs] = u;
+    if (u < 0) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(done_bar(hs));
       break;
     }
     const int b = (u / s.Hkv) % s.B, l = u / (s.Hkv * s.B);
@@ -1113,7 +1162,7 @@ static int fixed_bytes_split(const Shape& s, int splits, int max_tokens) {
 static int fixed_bytes_persistent(const Shape& s) {
   const HeaderLayout hl(s.G, s.D, s.WR);
   const int part = kPConsumers * s.G * (s.D + 2) * 4;
-  return 2 * hl.bytes + 2 * part + (2 * kPMaxStages + 8) * 8 + 16;
+  return 2 * hl.bytes + 2 * part + (2 * kPMaxStages + 8) * 8 + 32;
 }
 
 int attention_max_smem() { return 225 * 1024; }

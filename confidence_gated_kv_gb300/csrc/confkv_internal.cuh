@@ -138,7 +138,17 @@ struct Dev {
   int attn_ctas;                   // cap on the persistent attention grid (0 = none)
   long long* step_dev;             // decode steps done since prefill (read by prestep and select)
   uint32_t* sel_done;              // select CTAs finished in the current step (0 between steps)
+  int32_t* order;                  // [l*b] (layer, sequence) groups, most INT8 entries first
+                                   // (written by prestep when `sorted`)
+  int sorted;                      // prestep sorts the groups every step
+  int sched;                       // how the persistent attention kernel deals its units
+  uint32_t* queue;                 // next sorted position to hand out (kSchedQueue; zeroed by prestep)
 };
+
+enum : int { kSchedRoundRobin = 0, kSchedQueue = 1 };
+
+// Groups (layer, sequence) that prestep can sort by INT8 length in one block.
+constexpr int kSortMaxGroups = 1024;
 
 // Status bits written by kernels (never trap; the host reads them lazily).
 enum : int32_t {

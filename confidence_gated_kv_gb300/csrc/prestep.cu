@@ -162,6 +162,39 @@ __device__ void append_units(const Shape& s, const Dev& d, long long step_arg, i
   }
 }
 
+// The (layer, sequence) groups sorted by their INT8 length, longest first,
+// ties by index: d.order[rank] = group.  The attention kernel deals its units
+// to CTAs in snake order over this list, which balances the CTAs' streams
+// (a unit's time follows its bytes, and the INT8 region is the part of a
+// unit's length that varies).  The rank of a group is the number of groups
+// that sort before it; kSortPerBlock groups per block, four threads per
+// group each counting over a quarter of the keys.
+constexpr int kSortPerBlock = kConfThreads / 4;
+
+__device__ void order_block(const Shape& s, const Dev& d, int part) {
+  __shared__ int key[kSortMaxGroups];
+  const int n = s.L * s.B;
+  for (int i = threadIdx.x; i < n; i += kConfThreads) key[i] = d.n8[i];
+  __syncthreads();
+  const int i = part * kSortPerBlock + (threadIdx.x >> 2), q = threadIdx.x & 3;
+  int r = 0;
+  if (i < n) {
+    const int ki = key[i];
+    for (int j = q; j < n; j += 4) {
+      const int kj = key[j];
+      r += (kj > ki) | ((kj == ki) & (j < i));
+    }
+  }
+  r += __shfl_xor_sync(0xffffffffu, r, 1);
+  r += __shfl_xor_sync(0xffffffffu, r, 2);
+  if (i < n && q == 0) d.order[r] = i;
+  if (part == 0 && threadIdx.x == 0) *d.queue = 0u;
+}
+
+__host__ __device__ inline int sort_blocks(const Shape& s, const Dev& d) {
+  return d.sorted ? (s.L * s.B + kSortPerBlock - 1) / kSortPerBlock : 0;
+}
+
 constexpr int kAppendUnitsPerBlock = 4 * (kConfThreads / 32);
 
 template <int D, bool kDevStep>
@@ -173,6 +206,8 @@ __global__ void __launch_bounds__(kConfThreads) prestep_kernel(Shape s, Dev d, l
   pdl_wait();
   if ((int)blockIdx.x < nconf) {
     conf_block(s, d, logits, blockIdx.x / s.SV, blockIdx.x % s.SV);
+  } else if ((int)blockIdx.x >= (int)gridDim.x - sort_blocks(s, d)) {
+    order_block(s, d, (int)blockIdx.x - ((int)gridDim.x - sort_blocks(s, d)));
   } else {
     const int units = s.L * s.B * s.Hkv;
     const int u0 = ((int)blockIdx.x - nconf) * kAppendUnitsPerBlock;
@@ -184,7 +219,8 @@ int launch_prestep(const Shape& s, const Dev& d, long long step, const float* lo
                    const void* k_new, const void* v_new, bool conf, cudaStream_t stream) {
   const int units = s.L * s.B * s.Hkv;
   const int nconf = conf ? s.B * s.SV : 0;
-  const unsigned grid = (unsigned)(nconf + (units + kAppendUnitsPerBlock - 1) / kAppendUnitsPerBlock);
+  const unsigned grid =
+      (unsigned)(nconf + (units + kAppendUnitsPerBlock - 1) / kAppendUnitsPerBlock + sort_blocks(s, d));
   const __half* kn = static_cast<const __half*>(k_new);
   const __half* vn = static_cast<const __half*>(v_new);
   const dim3 g(grid), blk(kConfThreads);

@@ -32,7 +32,7 @@ EMA_TOL = 1e-5
 C_TOL = 1e-6
 TAU_BAND = 1e-6
 TIE_BAND = 1e-5
-MASS_RTOL = 1e-4
+MASS_RTOL = 1e-3
 F32_EPS = float(np.finfo(np.float32).eps)
 
 

@@ -105,6 +105,7 @@ def test_two_token_vocabulary_closed_form():
     lg = np.array([[z, 0.0] for z in zs], dtype=np.float32)
     closed = []
     for z in zs:
+        z = float(np.float32(z))           # the logit the kernels see
         p1 = 1.0 / (1.0 + np.exp(-abs(z)))
         p2 = 1.0 - p1
         h = -(p1 * np.log(p1) + (p2 * np.log(p2) if p2 > 0 else 0.0))

@@ -378,6 +378,7 @@ def run_ours(args):
         """Prefill, the untimed steps (at least W warm-up steps), then exactly
         K timed steps of one seeded instance of the workload."""
         cache = ck.Cache(cfg, device=dev)
+        cache.set_step_mode(ck.binding.STEP_SEPARATE if args.step_mode == "separate" else ck.binding.STEP_AUTO)
         k, v = prefill_batch_fast(w, seed, dev)
         cache.prefill(k, v, [w.T0] * w.B)
         torch.cuda.synchronize()
@@ -550,6 +551,7 @@ def run_ours(args):
             "kernel_timing": "CUDA events around each kernel on every %dth timed step (%d steps sampled)"
                              % (every, prof["steps"]),
             "attention_launch": {"ctas_per_unit": splits, "smem_bytes": smem},
+            "step_launches": cache.step_launches(), "step_mode": args.step_mode,
             "gpu_launches": int(st1["launches"] - st0["launches"]),
             "clocks": clk,
             "e2e": e2e,
@@ -682,6 +684,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--compaction", default="tailfill", choices=["tailfill", "ordered"],
                     help="INT8 compaction: tail fill (default) or the order-preserving ablation")
+    ap.add_argument("--step-mode", default="auto", choices=["auto", "separate"],
+                    help="auto: one fused launch per step where the shape allows it; separate: three kernels")
     ap.add_argument("--graph", action="store_true",
                     help="also time CUDA-graph replays of captured steps (extra 'graph' key)")
     ap.add_argument("--compare", action="store_true",

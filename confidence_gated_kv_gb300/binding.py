@@ -39,6 +39,7 @@ class Config(ctypes.Structure):
     ]
 
 COMPACT_TAIL_FILL, COMPACT_ORDERED = 0, 1
+STEP_AUTO, STEP_SEPARATE = 0, 1
 STATUS_CAPACITY, STATUS_EVICT_BOUND, STATUS_BAD_COUNT, STATUS_TIMEOUT = 1, 2, 4, 8
 
 
@@ -98,6 +99,8 @@ def lib() -> ctypes.CDLL:
                                     [ctypes.POINTER(i32)]),
             "confkv_attention_plan": (ctypes.c_int, [vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]),
             "confkv_set_attention_ctas": (ctypes.c_int, [vp, i32]),
+            "confkv_set_step_mode": (ctypes.c_int, [vp, i32]),
+            "confkv_step_launches": (ctypes.c_int, [vp, ctypes.POINTER(i32)]),
             "confkv_attention_grid": (ctypes.c_int, [vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]),
             "confkv_graph_reserve": (ctypes.c_int, [vp, i64]),
             "confkv_graph_advance": (ctypes.c_int, [vp, i64]),
@@ -388,6 +391,16 @@ class Cache:
         _check(lib().confkv_attention_plan(self._h, ctypes.byref(sp), ctypes.byref(sm)),
                "confkv_attention_plan")
         return int(sp.value), int(sm.value)
+
+    def set_step_mode(self, mode):
+        """STEP_AUTO (one launch per step where it fits) or STEP_SEPARATE."""
+        _check(lib().confkv_set_step_mode(self._h, int(mode)), "confkv_set_step_mode")
+
+    def step_launches(self) -> int:
+        """Kernel launches the next step takes (1: the fused step, 3 otherwise)."""
+        n = ctypes.c_int32()
+        _check(lib().confkv_step_launches(self._h, ctypes.byref(n)), "confkv_step_launches")
+        return int(n.value)
 
     def set_attention_ctas(self, ctas):
         """Cap the persistent attention grid at `ctas` CTAs (0: two per SM)."""

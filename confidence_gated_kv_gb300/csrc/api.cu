@@ -118,6 +118,7 @@ size_t layout(const Shape& s, char* base, Dev* d, Staging* st) {
   dd.sel_done = cv.take<uint32_t>(1);
   dd.order = cv.take<int32_t>(lbs);
   dd.queue = cv.take<uint32_t>(1);
+  dd.arrive = cv.take<uint32_t>(lbs);
   // the persistent attention kernel takes its units longest first from a
   // queue over prestep's sorted order (round robin when there are too many
   // groups to sort in one prestep launch)
@@ -157,6 +158,7 @@ struct confkv_ctx {
   int minN = 0, maxN = 0;
   long long host_h2d = 0, host_d2h = 0;   // bytes of the last confkv_step_host
   long long launches = 0;                  // kernels launched by decode steps
+  bool fused_ok = true;                    // small shapes may run a step as one launch
   // confkv_step_host: a second stream copies the attention output back while
   // the select kernel runs (created on first use)
   cudaStream_t aux = nullptr;
@@ -227,6 +229,7 @@ int confkv_create(const confkv_config* cfg, void* workspace, size_t workspace_by
   if (e == cudaSuccess) e = cudaMemset(c->d.step_dev, 0, sizeof(long long));
   if (e == cudaSuccess) e = cudaMemset(c->d.sel_done, 0, sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(c->d.conf_done, 0, s.B * sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaMemset(c->d.arrive, 0, (size_t)s.L * s.B * sizeof(uint32_t));
   if (e != cudaSuccess) {
     delete c;
     return CONFKV_ECUDA;
@@ -268,6 +271,7 @@ int confkv_prefill(confkv_ctx* ctx, const int32_t* prefill_len, const void* k, c
   if (e == cudaSuccess) e = cudaMemsetAsync(ctx->d.step_dev, 0, sizeof(long long), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(ctx->d.sel_done, 0, sizeof(uint32_t), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(ctx->d.conf_done, 0, s.B * sizeof(uint32_t), st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ctx->d.arrive, 0, (size_t)s.L * s.B * sizeof(uint32_t), st);
   if (e != cudaSuccess) return CONFKV_ECUDA;
   if (launch_prefill(s, ctx->d, k, v, t_max, ctx->T0.data(), st) != 0) return CONFKV_ECUDA;
   // the host copy of T0 is pageable: make sure it has been consumed
@@ -376,6 +380,21 @@ int confkv_attention_plan(confkv_ctx* ctx, int32_t* splits, int32_t* smem_bytes)
   return CONFKV_OK;
 }
 
+int confkv_set_step_mode(confkv_ctx* ctx, int32_t mode) {
+  if (!ctx || (mode != CONFKV_STEP_AUTO && mode != CONFKV_STEP_SEPARATE)) return CONFKV_EINVAL;
+  ctx->fused_ok = mode == CONFKV_STEP_AUTO;
+  return CONFKV_OK;
+}
+
+int confkv_step_launches(confkv_ctx* ctx, int32_t* launches) {
+  if (!ctx || !launches) return CONFKV_EINVAL;
+  int splits = 0, max_tokens = 0;
+  const int r = plan_attention(ctx, &splits, &max_tokens);
+  if (r != CONFKV_OK) return r;
+  *launches = ctx->fused_ok && fused_step_fits(ctx->s, ctx->d, splits, max_tokens) ? 1 : 3;
+  return CONFKV_OK;
+}
+
 int confkv_set_attention_ctas(confkv_ctx* ctx, int32_t ctas) {
   if (!ctx || ctas < 0) return CONFKV_EINVAL;
   ctx->d.attn_ctas = ctas;
@@ -446,6 +465,28 @@ static int step_impl(confkv_ctx* ctx, const void* q, const void* k_new, const vo
   // from the device counter, which the reservation set and each step advances
   const long long step_arg = (capturing || ctx->pin_left > 0) ? -1 : ctx->steps;
   const bool attn_conf = conf_in_attention && splits == 1;
+  // Small shapes: the whole step in one launch (attention.cu, fused mode),
+  // when every unit and vocabulary chunk gets a CTA of its own in one wave.
+  if (!conf_in_attention && !before_attention && ctx->fused_ok && fused_step_fits(s, ctx->d, splits, max_tokens)) {
+    if (prof) cudaEventRecord(ev[1], st);
+    if (launch_fused_step(s, ctx->d, step_arg, q, k_new, v_new, logits, out, budget, confidence, evicted_pos,
+                          n_evicted, max_tokens, st) != 0)
+      return CONFKV_ECUDA;
+    if (prof) {
+      cudaEventRecord(ev[2], st);
+      cudaEventRecord(ev[3], st);
+      ctx->prof_count++;
+    }
+    if (after_attention && cudaEventRecord(after_attention, st) != cudaSuccess) return CONFKV_ECUDA;
+    if (!capturing) {
+      ctx->launches += 1;
+      ctx->steps++;
+      ctx->n_bound = n_after;
+      ctx->n8_bound = n8_after;
+      if (ctx->pin_left > 0) ctx->pin_left--;
+    }
+    return CONFKV_OK;
+  }
   if (launch_prestep(s, ctx->d, step_arg, logits, k_new, v_new, !attn_conf, st) != 0) return CONFKV_ECUDA;
   if (prof) cudaEventRecord(ev[1], st);
   if (before_attention && cudaStreamWaitEvent(st, before_attention, 0) != cudaSuccess) return CONFKV_ECUDA;
@@ -821,8 +862,11 @@ int confkv_get_stats(confkv_ctx* ctx, confkv_stats* out, void* stream) {
   out->device_status = status;
   out->host_h2d_bytes = ctx->host_h2d;
   out->host_d2h_bytes = ctx->host_d2h;
-  out->peak_resident = (int64_t)ds.peak_entries;
-  out->peak_resident_bytes = (int64_t)ds.peak_bytes;
+  // the latest step's footprint is still in its accumulators (the next
+  // step folds it on the device)
+  const int last = (int)((ctx->steps + 1) & 1);
+  out->peak_resident = (int64_t)std::max(ds.peak_entries, ctx->steps > 0 ? ds.res_entries_acc[last] : 0ull);
+  out->peak_resident_bytes = (int64_t)std::max(ds.peak_bytes, ctx->steps > 0 ? ds.res_bytes_acc[last] : 0ull);
   out->workspace_bytes = (int64_t)ctx->ws_bytes;
   out->launches = ctx->launches;
   return status ? CONFKV_EDEVICE : CONFKV_OK;

@@ -41,6 +41,7 @@
 #include <cooperative_groups.h>
 #include <cfloat>
 #include "confidence_merge.cuh"
+#include "select_body.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -782,17 +783,55 @@ __device__ __forceinline__ int unit_of_rank(const Shape& s, const Dev& d, int un
 //                     remaining units: the longest-first queue evens out the
 //                     CTAs' end times.
 //   kSchedRoundRobin  u = blockIdx.x + k * gridDim.x (groups not sorted).
+//   fused step        CTA i < units takes unit i, and only that one.
+template <bool kFused>
 __device__ __forceinline__ int next_unit(const Shape& s, const Dev& d, int units, int k) {
+  if (kFused) return (k == 0 && (int)blockIdx.x < units) ? (int)blockIdx.x : -1;
   if (d.sched == kSchedQueue) return unit_of_rank(s, d, units, (int)atomicAdd(d.queue, 1u));
   const int u = (int)blockIdx.x + k * (int)gridDim.x;
   return u < units ? u : -1;
 }
 
-template <int D, bool kFlush>
+// Modes of the persistent kernel.
+//   kModeAttention    attention and mass only (prestep and select run as
+//                     kernels of their own);
+//   kModeFused        the whole decode step in one launch for shapes whose
+//                     units and vocabulary chunks fit one wave: CTAs
+//                     [0, units) take one unit each and append its new token
+//                     first; CTAs [units, units + B * SV) reduce one
+//                     vocabulary chunk each, and the last chunk of a sequence
+//                     merges its confidence and budgets.  Each (layer,
+//                     sequence) counts Hkv unit arrivals and one confidence
+//                     arrival; the CTA that makes the last one runs that
+//                     group's selection (select_body.cuh) once its own work is
+//                     done.  No CTA waits for another.
+//   kModeFusedDevStep the same, with the step index read from the device (a
+//                     step inside a graph reservation).
+enum : int { kModeAttention = 0, kModeFused = 1, kModeFusedDevStep = 2 };
+
+// What a fused step needs beyond the attention arguments.
+struct FusedArgs {
+  long long step;                 // step index (kModeFused)
+  const __half* k_new;            // [L][B][Hkv][D]
+  const __half* v_new;
+  int32_t* evicted;               // [L][B][max_evict]
+  int32_t* nevict;                // [L][B]
+  SelSmem sm;                     // selection layout, at offset kFusedSelOff of the stage area
+};
+
+// Shared memory of a selection inside the fused kernel (after the CTA's own
+// work, reusing the stage area): SelShared at 0, the selection's dynamic
+// layout from kFusedSelOff.
+constexpr int kFusedSelOff = 2048;
+static_assert(sizeof(SelShared) <= kFusedSelOff, "SelShared fits below the selection area");
+
+template <int D, bool kFlush, int kMode>
 __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
     Shape s, Dev d, const void* __restrict__ q, float* __restrict__ out,
     int32_t* __restrict__ budget, float* __restrict__ conf_out, const float* __restrict__ logits,
-    int stages) {
+    int stages, FusedArgs fa) {
+  constexpr bool kFused = kMode != kModeAttention;
+  constexpr bool kDevStep = kMode == kModeFusedDevStep;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   constexpr int kStageBytes = 128 * D;
   constexpr int kHalf = kStageBytes / 2;
@@ -803,13 +842,18 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
   float* wpart = reinterpret_cast<float*>(hbuf + 2 * hl.bytes);            // [2][4][G][D + 2]
   const int part_floats = kPConsumers * G * (D + 2);
   uint64_t* bars = reinterpret_cast<uint64_t*>(wpart + 2 * part_floats);
-  int* s_misc = reinterpret_cast<int*>(bars + 2 * kPMaxStages + 8);
+  int* s_misc = reinterpret_cast<int*>(bars + 2 * kPMaxStages + 10);
   int& s_abort = s_misc[0];
   // unit index of header slot hs (set by the producer before its arrival on
   // hfull) and of partials slot ps (set by consumer warp 0 before its arrival
   // on done); -1 ends the CTA's work
   volatile int* s_unit = s_misc + 1;    // [2]
   volatile int* s_eunit = s_misc + 3;   // [2]
+  // fused step: the (layer, sequence) whose selection falls to this CTA, -1 if none
+  volatile int* s_sel = s_misc + 5;
+  // fused step: the unit's Mg[8], 1 / Lg[8] for the consumer warps' share of
+  // the mass loop
+  float* s_mass = reinterpret_cast<float*>(s_misc + 8);
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
   auto empty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(kPMaxStages + i); };
@@ -817,6 +861,10 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
   auto hempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * kPMaxStages + 2 + i); };
   auto done_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * kPMaxStages + 4 + i); };
   auto efree_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * kPMaxStages + 6 + i); };
+  // fused step: s_mass published (1 arrival), the mass loop shared by the
+  // consumer warps and the epilogue warp done (5 arrivals)
+  const uint32_t mready_bar = bar0 + 8u * (uint32_t)(2 * kPMaxStages + 8);
+  const uint32_t mdone_bar = bar0 + 8u * (uint32_t)(2 * kPMaxStages + 9);
   // this CTA's two score slots: [2][G][S] (token index = slot index in the unit)
   float* scg_base = d.scores + (size_t)blockIdx.x * 2 * G * s.S;
 
@@ -826,8 +874,59 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
   const int g = lane >> 2, t = lane & 3;
 
   pdl_wait();
+  // fused step: the step index of the new token and of the selections
+  const long long fstep = kDevStep ? __ldcg(d.step_dev) : fa.step;
+  if constexpr (kFused) {
+    if ((int)blockIdx.x >= units) {
+      // ------------------------------------------------ vocabulary CTA
+      // one chunk of one sequence's logits; the CTA that completes a
+      // sequence's chunks merges its confidence and budgets, then counts one
+      // arrival on every layer of the sequence
+      const int c = (int)blockIdx.x - units;
+      const int b = c / s.SV;
+      unsigned char* vs = smem_raw + kFusedSelOff + ((fa.sm.bytes + 127) & ~127);
+      ConfAcc* red = reinterpret_cast<ConfAcc*>(vs);                          // [6]
+      int* s_list = reinterpret_cast<int*>(vs + 6 * sizeof(ConfAcc));        // [L]
+      int* s_n = s_list + s.L;                                                // [2]
+      conf_partial_block<kPThreads / 32>(s, d, logits, b, c % s.SV, red);
+      if (threadIdx.x == 0) {
+        __threadfence();
+        s_n[0] = atomicAdd(d.conf_done + b, 1u) == (unsigned)s.SV - 1u;
+        s_n[1] = 0;
+      }
+      __syncthreads();
+      if (!s_n[0]) return;
+      if (warp == 0) {
+        __threadfence();
+        conf_merge_warp(s, d, b, budget, conf_out);
+        if (lane == 0) d.conf_done[b] = 0u;   // zero again for the next launch
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        __threadfence();
+        int n = 0;
+        for (int l = 0; l < s.L; ++l) {
+          const int lb = l * s.B + b;
+          if (atomicAdd(d.arrive + lb, 1u) == (unsigned)s.Hkv) s_list[n++] = lb;
+        }
+        s_n[1] = n;
+        __threadfence();
+      }
+      __syncthreads();
+      SelShared& sh = *reinterpret_cast<SelShared*>(smem_raw);
+      for (int i = 0; i < s_n[1]; ++i) {
+        const int lb = s_list[i];
+        if (threadIdx.x == 0) d.arrive[lb] = 0u;   // every arrival of this step is in
+        select_group<D, true, kDevStep, false, kPThreads, false>(s, d, fstep, lb, fa.evicted, fa.nevict, fa.sm,
+                                                          smem_raw + kFusedSelOff, sh);
+        __syncthreads();
+      }
+      return;
+    }
+  }
   if (threadIdx.x == 0) {
     s_abort = 0;
+    s_sel[0] = -1;
     for (int i = 0; i < stages; ++i) {
       mbar_init(full_bar(i), 1);
       mbar_init(empty_bar(i), kPConsumers);
@@ -838,6 +937,8 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
       mbar_init(done_bar(i), kPConsumers);
       mbar_init(efree_bar(i), 1);
     }
+    mbar_init(mready_bar, 1);
+    mbar_init(mdone_bar, kPConsumers + 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
@@ -848,13 +949,75 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
   };
   auto aborted = [&](void) { return *(volatile int*)&s_abort != 0; };
 
+  // End of this CTA's work: in a fused step, every warp meets here once its
+  // role is done, and if this CTA made the last arrival of a (layer,
+  // sequence) the whole CTA runs that group's selection over the stage
+  // area (every bulk copy into it has landed: the producer waited for them).
+  auto finish = [&](void) {
+    if constexpr (kFused) {
+      __syncthreads();
+      const int lb = s_sel[0];
+      if (lb >= 0 && !aborted()) {
+        __threadfence();
+        if (threadIdx.x == 0) d.arrive[lb] = 0u;   // every arrival of this step is in
+        SelShared& sh = *reinterpret_cast<SelShared*>(smem_raw);
+        select_group<D, true, kDevStep, false, kPThreads, false>(s, d, fstep, lb, fa.evicted, fa.nevict, fa.sm,
+                                                          smem_raw + kFusedSelOff, sh);
+      }
+    }
+  };
+
+  // Per-token attention mass of unit u from its raw scores in score slot
+  // scg, over the quads (4 consecutive slots; slot groups never straddle the
+  // INT8 / ring boundary) first, first + stride, ...; empty slots get 0
+  // (never read).  The scores are read once: streaming loads (evict-first,
+  // coherent) keep them from displacing L1 lines the consumer warps use;
+  // plain cached loads here cost the kernel ~8 us per launch on the
+  // Qwen-32B shape.
+  auto mass_quads = [&](int u, int nb8, const float* scg, const float (&Mg)[kMaxG], const float (&invL)[kMaxG],
+                        int first, int stride) {
+    float* mass_u = d.mass + (size_t)u * s.S;
+    const int nq = (nb8 * 16 + s.WR) / 4;
+    for (int i = first; i < nq; i += stride) {
+      const int v = 4 * i;
+      const int slot = v < nb8 * 16 ? v : s.cap + (v - nb8 * 16);
+      float4 sv[kMaxG];
+#pragma unroll
+      for (int gg = 0; gg < kMaxG; ++gg)
+        if (gg < G) sv[gg] = __ldcs(reinterpret_cast<const float4*>(scg + (size_t)gg * s.S + slot));
+      float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int gg = 0; gg < kMaxG; ++gg) {
+        if (gg < G) {
+          m.x += ex2(sv[gg].x - Mg[gg]) * invL[gg];
+          m.y += ex2(sv[gg].y - Mg[gg]) * invL[gg];
+          m.z += ex2(sv[gg].z - Mg[gg]) * invL[gg];
+          m.w += ex2(sv[gg].w - Mg[gg]) * invL[gg];
+        }
+      }
+      *reinterpret_cast<float4*>(mass_u + slot) = m;
+    }
+  };
+
   if (warp == kPConsumers) {
     // ------------------------------------------------ producer warp
+    if constexpr (kFused) {
+      // the new token of this CTA's unit goes to its ring slot before the
+      // unit's header and blocks are read; the proxy fence orders these
+      // stores before the bulk copies (async proxy) that read them back
+      if ((int)blockIdx.x < units) {
+        const int u = blockIdx.x;
+        const int b = (u / s.Hkv) % s.B;
+        append_unit_warp<D>(s, d, u, d.T0[b] + (int)fstep, fa.k_new, fa.v_new);
+      }
+      asm volatile("fence.proxy.async.global;\n" ::: "memory");
+      __syncwarp();
+    }
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       RingPos st;
       long long issued = 0;
-      int u = next_unit(s, d, units, 0);
+      int u = next_unit<kFused>(s, d, units, 0);
       for (int k = 0; !aborted(); ++k) {
         const int hs = k & 1;
         if (k >= 2 && !mbar_wait(hempty_bar(hs), (uint32_t)(((k >> 1) - 1) & 1))) { fail(); break; }
@@ -902,10 +1065,10 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
           st.next(stages);
           ++issued;
           // the next unit is known early, so a queue's atomic stays off the stream
-          if (i == 0) u_next = next_unit(s, d, units, k + 1);
+          if (i == 0) u_next = next_unit<kFused>(s, d, units, k + 1);
         }
         if (!ok) { fail(); break; }
-        u = sch.nst > 0 ? u_next : next_unit(s, d, units, k + 1);
+        u = sch.nst > 0 ? u_next : next_unit<kFused>(s, d, units, k + 1);
       }
       // wait (bounded) for the last copy of every stage slot: nothing may be
       // in flight into shared memory when the CTA's threads have all exited
@@ -916,13 +1079,14 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
         if (!mbar_wait(full_bar(dr.slot), dr.phase)) atomicOr(d.status, kStatusTimeout);
       }
     }
+    finish();
     return;
   }
 
   if (warp == kPConsumers + 1) {
     // ------------------------------------------------ epilogue warp
     // Idle until the first unit is done: the confidence of the step.
-    if (logits) {
+    if (!kFused && logits) {
       // Logits in host memory: this CTA reduces its vocabulary chunks to
       // partials here, so that their transfer overlaps the attention; the
       // CTA that finishes the last chunk of a sequence merges that sequence.
@@ -941,7 +1105,7 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
           if (lane == 0) d.conf_done[b] = 0u;   // zero again for the next launch
         }
       }
-    } else {
+    } else if (!kFused) {
       // the prestep kernel wrote the partials: merge the sequences this CTA owns
       for (int b = blockIdx.x; b < s.B; b += gridDim.x) conf_merge_warp(s, d, b, budget, conf_out);
     }
@@ -987,40 +1151,37 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
           }
         }
       }
-      // attention mass, 4 consecutive slots per lane (slot groups never
-      // straddle the INT8 / ring boundary); empty slots get 0 (never read)
+      // attention mass of the unit's tokens
       const float* scg = scg_base + (size_t)ps * G * s.S;
-      float* mass_u = d.mass + (size_t)u * s.S;
-      const int nq = (nb8 * 16 + s.WR) / 4;
       float invL[kMaxG];
 #pragma unroll
       for (int gg = 0; gg < kMaxG; ++gg) invL[gg] = gg < G ? 1.0f / Lg[gg] : 0.f;
-      // The scores are read once: streaming loads (evict-first, coherent)
-      // keep them from displacing L1 lines the consumer warps use; plain
-      // cached loads here cost the kernel ~8 us per launch on the Qwen-32B
-      // shape.
-      for (int i = lane; i < nq; i += 32) {
-        const int v = 4 * i;
-        const int slot = v < nb8 * 16 ? v : s.cap + (v - nb8 * 16);
-        float4 sv[kMaxG];
+      if constexpr (kFused) {
+        // this CTA's only unit: the four consumer warps, idle now, take four
+        // fifths of the mass loop; the arrival on the unit's (layer,
+        // sequence) follows every share
+        if (lane == 0) {
 #pragma unroll
-        for (int gg = 0; gg < kMaxG; ++gg)
-          if (gg < G) sv[gg] = __ldcs(reinterpret_cast<const float4*>(scg + (size_t)gg * s.S + slot));
-        float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int gg = 0; gg < kMaxG; ++gg) {
-          if (gg < G) {
-            m.x += ex2(sv[gg].x - Mg[gg]) * invL[gg];
-            m.y += ex2(sv[gg].y - Mg[gg]) * invL[gg];
-            m.z += ex2(sv[gg].z - Mg[gg]) * invL[gg];
-            m.w += ex2(sv[gg].w - Mg[gg]) * invL[gg];
+          for (int gg = 0; gg < kMaxG; ++gg) {
+            s_mass[gg] = Mg[gg];
+            s_mass[kMaxG + gg] = invL[gg];
           }
+          mbar_arrive(mready_bar);
         }
-        *reinterpret_cast<float4*>(mass_u + slot) = m;
+        mass_quads(u, nb8, scg, Mg, invL, kPConsumers * 32 + lane, (kPConsumers + 1) * 32);
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(mdone_bar);
+        if (!mbar_wait(mdone_bar, 0)) fail();
+        __threadfence();
+        if (lane == 0 && !aborted() && atomicAdd(d.arrive + lb, 1u) == (unsigned)s.Hkv) s_sel[0] = (int)lb;
+      } else {
+        mass_quads(u, nb8, scg, Mg, invL, lane, 32);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(efree_bar(ps));
     }
+    finish();
     return;
   }
 
@@ -1139,6 +1300,30 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
       mbar_arrive(hempty_bar(hs));
     }
   }
+  if constexpr (kFused) {
+    // the consumer warps' share of the mass loop of this CTA's only unit
+    // (unit index in header slot 0), once the epilogue warp has published
+    // the unit's maxima and normalisers
+    const int u0 = s_unit[0];
+    if (u0 >= 0 && !aborted()) {
+      if (mbar_wait(mready_bar, 0)) {
+        float Mg[kMaxG], invL[kMaxG];
+#pragma unroll
+        for (int gg = 0; gg < kMaxG; ++gg) {
+          Mg[gg] = s_mass[gg];
+          invL[gg] = s_mass[kMaxG + gg];
+        }
+        const int nb8 = (d.n8[u0 / s.Hkv] + 15) >> 4;
+        mass_quads(u0, nb8, scg_base, Mg, invL, (int)threadIdx.x, (kPConsumers + 1) * 32);
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(mdone_bar);
+      } else {
+        fail();
+      }
+    }
+  }
+  finish();
 }
 
 // ---------------------------------------------------------------------------
@@ -1162,7 +1347,7 @@ static int fixed_bytes_split(const Shape& s, int splits, int max_tokens) {
 static int fixed_bytes_persistent(const Shape& s) {
   const HeaderLayout hl(s.G, s.D, s.WR);
   const int part = kPConsumers * s.G * (s.D + 2) * 4;
-  return 2 * hl.bytes + 2 * part + (2 * kPMaxStages + 8) * 8 + 32;
+  return 2 * hl.bytes + 2 * part + (2 * kPMaxStages + 10) * 8 + 96;
 }
 
 int attention_max_smem() { return 225 * 1024; }
@@ -1266,12 +1451,13 @@ static int launch_d(const Shape& s, const Dev& d, const void* q, float* out, int
     // at its register limit (0.292 against 0.285 ms on the Qwen-32B shape).
     static int configured[2][kMaxDevices] = {};
     const bool flush = max_tokens - s.WR > kFlushTokens;
-    auto kern = flush ? attention_persistent_kernel<D, true> : attention_persistent_kernel<D, false>;
+    auto kern = flush ? attention_persistent_kernel<D, true, kModeAttention>
+                      : attention_persistent_kernel<D, false, kModeAttention>;
     if (ensure_smem(kern, attention_max_smem(), configured[flush]) != cudaSuccess) return -1;
     int grid = 0, cluster = 0;
     attention_grid(s, d, 1, &grid, &cluster);
     return launch_pdl(kern, dim3(grid), dim3(kPThreads), (size_t)smem, stream, s, d, q, out, budget,
-                      conf_out, logits, stages_persistent(s)) == cudaSuccess
+                      conf_out, logits, stages_persistent(s), FusedArgs{}) == cudaSuccess
                ? 0
                : -1;
   }
@@ -1292,6 +1478,61 @@ static int launch_d(const Shape& s, const Dev& d, const void* q, float* out, int
   cudaError_t e = cudaLaunchKernelEx(&cfg, attention_kernel<D>, s, d, q, out, budget, conf_out,
                                      splits, chunk, stages_split(s, splits, max_tokens));
   return e == cudaSuccess ? 0 : -1;
+}
+
+// A fused step: every unit on a CTA of its own next to one CTA per
+// vocabulary chunk, all in one wave of the persistent grid; units short
+// enough for the instance without the INT8 V bias flush; tail-fill
+// compaction; and the selection's keys and bitmaps inside the stage area.
+bool fused_step_fits(const Shape& s, const Dev& d, int splits, int max_tokens) {
+  const long long units = (long long)s.L * s.B * s.Hkv;
+  if (splits != 1 || s.compaction != 0) return false;
+  if (units + (long long)s.B * s.SV > attention_persistent_ctas()) return false;
+  if (d.attn_ctas > 0 && units + (long long)s.B * s.SV > d.attn_ctas) return false;
+  if (units > d.score_ctas) return false;
+  if (max_tokens - s.WR > kFlushTokens) return false;
+  const SelSmem sm = plan_select(s);
+  if (sm.off_key < 0) return false;
+  const long long need = kFusedSelOff + ((sm.bytes + 127) & ~127) + 6 * (long long)sizeof(ConfAcc) +
+                         4LL * (s.L + 2);
+  return need <= (long long)stages_persistent(s) * stage_bytes(s.D);
+}
+
+template <int D>
+static int launch_fused_d(const Shape& s, const Dev& d, long long step, const void* q, const void* k_new,
+                          const void* v_new, const float* logits, float* out, int32_t* budget, float* conf_out,
+                          int32_t* evicted_pos, int32_t* n_evicted, cudaStream_t stream) {
+  static int configured[2][kMaxDevices] = {};
+  const bool dev = step < 0;
+  auto kern = dev ? attention_persistent_kernel<D, false, kModeFusedDevStep>
+                  : attention_persistent_kernel<D, false, kModeFused>;
+  if (ensure_smem(kern, attention_max_smem(), configured[dev]) != cudaSuccess) return -1;
+  const int smem = stages_persistent(s) * stage_bytes(D) + fixed_bytes_persistent(s);
+  const int grid = s.L * s.B * s.Hkv + s.B * s.SV;
+  FusedArgs fa{};
+  fa.step = step;
+  fa.k_new = static_cast<const __half*>(k_new);
+  fa.v_new = static_cast<const __half*>(v_new);
+  fa.evicted = evicted_pos;
+  fa.nevict = n_evicted;
+  fa.sm = plan_select(s);
+  return launch_pdl(kern, dim3(grid), dim3(kPThreads), (size_t)smem, stream, s, d, q, out, budget, conf_out,
+                    logits, stages_persistent(s), fa) == cudaSuccess
+             ? 0
+             : -1;
+}
+
+int launch_fused_step(const Shape& s, const Dev& d, long long step, const void* q, const void* k_new,
+                      const void* v_new, const float* logits, float* out, int32_t* budget, float* conf_out,
+                      int32_t* evicted_pos, int32_t* n_evicted, int max_tokens, cudaStream_t stream) {
+  if (!fused_step_fits(s, d, 1, max_tokens)) return -1;
+  if (s.D == 128)
+    return launch_fused_d<128>(s, d, step, q, k_new, v_new, logits, out, budget, conf_out, evicted_pos,
+                               n_evicted, stream);
+  if (s.D == 64)
+    return launch_fused_d<64>(s, d, step, q, k_new, v_new, logits, out, budget, conf_out, evicted_pos,
+                              n_evicted, stream);
+  return -1;
 }
 
 int launch_attention(const Shape& s, const Dev& d, const void* q, float* out, int32_t* budget,

@@ -134,6 +134,100 @@ __device__ __forceinline__ void conf_partial_warp(const Shape& s, const Dev& d,
   }
 }
 
+// One warp's share [v0, v1) of a vocabulary chunk of row z, reduced to the
+// chunk partial's fields (every lane returns the warp's values, relative to
+// the warp maximum M).  Same single pass as conf_partial_warp.
+struct ConfAcc {
+  float M;
+  FSum S, T;
+  Top2 tp;
+};
+
+__device__ __forceinline__ ConfAcc conf_range_warp(const float* __restrict__ z, int v0, int v1) {
+  constexpr int kIn = 8;   // loads in flight per lane
+  const int lane = threadIdx.x & 31;
+  float m = -FLT_MAX;
+  FSum S{0.f, 0.f}, T{0.f, 0.f};
+  Top2 tp{-FLT_MAX, -FLT_MAX, 0x7fffffff};
+  for (int base = v0; base < v1; base += 32 * kIn) {
+    float x[kIn];
+#pragma unroll
+    for (int j = 0; j < kIn; ++j) {
+      const int idx = base + 32 * j + lane;
+      x[j] = idx < v1 ? __ldg(z + idx) : -FLT_MAX;
+    }
+#pragma unroll
+    for (int j = 0; j < kIn; ++j) {
+      const int idx = base + 32 * j + lane;
+      if (idx < v1) {
+        if (x[j] > m) {
+          conf_rescale(S, T, m, x[j]);
+          m = x[j];
+        }
+        const float dz = x[j] - m;
+        const float e = expf(dz);
+        S = fsum_add(S, e);
+        T = fsum_add(T, dz * e);
+        tp = top2_merge(tp, Top2{x[j], -FLT_MAX, idx});
+      }
+    }
+  }
+  float M = m;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  conf_rescale(S, T, m, M);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    S = fsum_add(S, fsum_shfl_xor(S, o));
+    T = fsum_add(T, fsum_shfl_xor(T, o));
+    Top2 other{__shfl_xor_sync(0xffffffffu, tp.z1, o), __shfl_xor_sync(0xffffffffu, tp.z2, o),
+               __shfl_xor_sync(0xffffffffu, tp.i1, o)};
+    tp = top2_merge(tp, other);
+  }
+  return ConfAcc{M, S, T, tp};
+}
+
+// Partial of vocabulary chunk `part` of sequence b computed by a whole block
+// of NW warps: each warp reduces a contiguous share of the chunk, then
+// thread 0 brings the warps' sums to the chunk maximum and adds them.
+// `red` holds NW ConfAcc in shared memory.  Called by every thread.
+template <int NW>
+__device__ __forceinline__ void conf_partial_block(const Shape& s, const Dev& d, const float* __restrict__ logits,
+                                                   int b, int part, ConfAcc* red) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int V = s.V;
+  const int chunk = (V + s.SV - 1) / s.SV;
+  const int v0 = part * chunk, v1 = min(V, v0 + chunk);
+  const int share = ((max(v1 - v0, 0) + NW - 1) / NW + 31) / 32 * 32;
+  const int w0 = min(v1, v0 + warp * share), w1 = min(v1, w0 + share);
+  const ConfAcc a = conf_range_warp(logits + (size_t)b * V, w0, w1);
+  if (lane == 0) red[warp] = a;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float M = -FLT_MAX;
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, red[w].M);
+    FSum S{0.f, 0.f}, T{0.f, 0.f};
+    Top2 tp{-FLT_MAX, -FLT_MAX, 0x7fffffff};
+    for (int w = 0; w < NW; ++w) {
+      FSum Sw = red[w].S, Tw = red[w].T;
+      conf_rescale(Sw, Tw, red[w].M, M);
+      S = fsum_add(S, Sw);
+      T = fsum_add(T, Tw);
+      tp = top2_merge(tp, red[w].tp);
+    }
+    ConfPartial cp;
+    cp.M = (v1 > v0) ? M : -FLT_MAX;
+    cp.z1 = tp.z1;
+    cp.z2 = tp.z2;
+    cp.i1 = tp.i1;
+    cp.S = S.hi;
+    cp.Se = S.lo;
+    cp.T = T.hi;
+    cp.Te = T.lo;
+    d.conf[(size_t)b * s.SV + part] = cp;
+  }
+}
+
 static_assert(sizeof(ConfPartial) == 32, "ConfPartial is read as two 16-byte words");
 
 // One chunk partial read from L2 (written by other CTAs of the same kernel

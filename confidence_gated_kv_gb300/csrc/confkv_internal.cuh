@@ -96,12 +96,13 @@ struct DevStats {        // cumulative counters, updated with atomics
   unsigned long long requant;
   unsigned long long attn_bytes;   // algorithmic bytes of the attention kernel
   unsigned long long step_bytes;   // algorithmic bytes of the whole step
-  // resident footprint after each step: every select CTA adds its (layer,
-  // sequence)'s entries and K/V bytes; the last CTA of the step takes the
-  // sums, keeps their maximum over steps and zeroes them for the next step
-  unsigned long long res_entries_acc, res_bytes_acc;
+  // resident footprint after each step: every selection adds its (layer,
+  // sequence)'s entries and K/V bytes to the accumulators of the step's
+  // parity; the first selection of the next step (group 0) folds them into
+  // the peaks and zeroes them, and confkv_get_stats folds the latest step's
+  // on the host, so no selection waits on another
+  unsigned long long res_entries_acc[2], res_bytes_acc[2];
   unsigned long long peak_entries, peak_bytes;
-  unsigned long long sel_arrivals;
 };
 
 struct Shape {
@@ -143,6 +144,7 @@ struct Dev {
   int sorted;                      // prestep sorts the groups every step
   int sched;                       // how the persistent attention kernel deals its units
   uint32_t* queue;                 // next sorted position to hand out (kSchedQueue; zeroed by prestep)
+  uint32_t* arrive;                // [l*b] fused steps: units and confidence of (l, b) done this step
 };
 
 enum : int { kSchedRoundRobin = 0, kSchedQueue = 1 };
@@ -215,6 +217,42 @@ inline cudaError_t ensure_smem(void (*kernel)(KArgs...), int bytes, int (&done)[
 }
 #endif
 
+#ifdef __CUDACC__
+// Append the new token of unit u = (l, b, kvh) at position t to its FP16 ring
+// slot t mod WR (rainbus Algorithm 1 step 13), by one whole warp: lane i
+// writes the 8 bytes of K that hold channels 16(i/4) + 2(i%4) + {0, 1, 8, 9}
+// of the interleaved block and V channels i, i + 32, ...; lane 0 writes the
+// slot's position and a zero EMA (the same values for every KV head of the
+// group).
+template <int D>
+__device__ __forceinline__ void append_unit_warp(const Shape& s, const Dev& d, int u, int t,
+                                                 const __half* __restrict__ k_new,
+                                                 const __half* __restrict__ v_new) {
+  const int lane = threadIdx.x & 31;
+  const int kc0 = 16 * (lane >> 2) + 2 * (lane & 3);
+  const int lbi = u / s.Hkv;
+  const int rs = t % s.WR;
+  const size_t blk = ((size_t)u * (s.WR / 16) + (rs >> 4)) * 16 * D * 2;
+  const unsigned short* kn = reinterpret_cast<const unsigned short*>(k_new) + (size_t)u * D;
+  const unsigned short* vn = reinterpret_cast<const unsigned short*>(v_new) + (size_t)u * D;
+  char* k16b = reinterpret_cast<char*>(d.k16);
+  char* v16b = reinterpret_cast<char*>(d.v16);
+  if (lane < D / 4) {
+    uint2 kx;
+    kx.x = *reinterpret_cast<const uint32_t*>(kn + kc0);
+    kx.y = *reinterpret_cast<const uint32_t*>(kn + kc0 + 8);
+    *reinterpret_cast<uint2*>(k16b + blk + k16_offset(D, rs & 15, kc0)) = kx;
+  }
+#pragma unroll
+  for (int i = 0; i < D / 32; ++i)
+    *reinterpret_cast<unsigned short*>(v16b + blk + v16_offset(D, rs & 15, lane + 32 * i)) = vn[lane + 32 * i];
+  if (lane == 0) {
+    d.pos[(size_t)lbi * s.S + s.cap + rs] = t;
+    d.ema[(size_t)lbi * s.S + s.cap + rs] = 0.f;
+  }
+}
+#endif
+
 // ---------------------------------------------------------------------------
 // Kernel launchers (defined in the .cu files; all asynchronous on `stream`).
 // ---------------------------------------------------------------------------
@@ -240,6 +278,13 @@ void attention_grid(const Shape& s, const Dev& d, int splits, int* grid, int* cl
 int launch_select(const Shape& s, const Dev& d, long long step, int32_t* evicted_pos,
                   int32_t* n_evicted, cudaStream_t stream);
 int attention_smem_bytes(const Shape& s, int splits, int max_tokens);
+// Fused step: one launch for the whole decode step (append, vocabulary
+// reduction and confidence, attention with mass, and every selection) when
+// fused_step_fits; step as for launch_prestep.
+bool fused_step_fits(const Shape& s, const Dev& d, int splits, int max_tokens);
+int launch_fused_step(const Shape& s, const Dev& d, long long step, const void* q, const void* k_new,
+                      const void* v_new, const float* logits, float* out, int32_t* budget, float* conf_out,
+                      int32_t* evicted_pos, int32_t* n_evicted, int max_tokens, cudaStream_t stream);
 int attention_max_smem();
 int attention_persistent_ctas();   // persistent CTAs per launch (2 per SM)
 int launch_selftest_timeout(const Dev& d, cudaStream_t stream);

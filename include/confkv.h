@@ -309,6 +309,26 @@ int confkv_profile_read(confkv_ctx* ctx, double* ms_prestep, double* ms_attentio
  * without a context. */
 int confkv_attention_plan(confkv_ctx* ctx, int32_t* splits, int32_t* smem_bytes);
 
+/* How confkv_step runs a step on the device (results do not depend on it):
+ *   CONFKV_STEP_AUTO (default)  one kernel launch for the whole step when
+ *       every (layer, sequence, KV head) unit and every 4096-logit chunk of
+ *       the vocabulary can have a CTA of its own in one wave of the
+ *       persistent attention grid (two per SM), the INT8 region of a unit
+ *       stays within 8192 tokens, compaction is tail fill, the selection's
+ *       working set fits the kernel's shared memory and the logits are in
+ *       device memory; otherwise three launches;
+ *   CONFKV_STEP_SEPARATE  always three launches (confidence reduction and
+ *       append; attention; selection).
+ * The fused launch removes two kernel launches and their gaps from steps of
+ * small shapes (the pages' per-step profile, [rainbus] 复现评估, is
+ * dominated by such fixed costs there).  confkv_step_launches gives the
+ * launches the next step would take.  CONFKV_EINVAL for a null ctx or an
+ * unknown mode.  The pages give no counterpart: these are launch controls of
+ * this library. */
+enum { CONFKV_STEP_AUTO = 0, CONFKV_STEP_SEPARATE = 1 };
+int confkv_set_step_mode(confkv_ctx* ctx, int32_t mode);
+int confkv_step_launches(confkv_ctx* ctx, int32_t* launches);
+
 /* Caps the attention grid at `ctas` CTAs; 0 (the default) lets the
  * persistent kernel use two CTAs per SM.  The split-K kernel is chosen only
  * while units x splits stays within the cap, otherwise the persistent kernel

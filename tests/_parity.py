@@ -151,7 +151,7 @@ class Pair:
     """CUDA cache + oracle driven by the same inputs."""
 
     def __init__(self, w, seed: int, prefill_len=None, cap=None, max_evict=0, k=None, v=None,
-                 compaction=0):
+                 compaction=0, mode=0):
         self.w = w
         self.seed = seed
         self.prm = orc.Params.from_workload(w)
@@ -163,7 +163,9 @@ class Pair:
         self.oracle.prefill(k, v, self.T0)
         self.cache = ck.Cache(ck.config_from_workload(w, cap=cap, max_evict=max_evict, compaction=compaction))
         self.cache.prefill(k.cuda(), v.cuda(), self.T0)
+        self.cache.set_step_mode(mode)
         self.flags = Flags()
+        self.launches = 0          # kernel launches the plain steps took (the library's count)
         self.exports = {}          # (b, l) -> last GPU export that matched the oracle
         self.peak_entries = 0      # largest oracle resident count after a step
         self.peak_bytes = 0
@@ -215,6 +217,7 @@ class Pair:
         plain cache.step call (graph replays) and returns the output dict."""
         w = self.w
         if gpu_step is None:
+            self.launches += self.cache.step_launches()
             o = self.cache.step(q.cuda(), kn.cuda(), vn.cuda(), lg.cuda())
         else:
             o = gpu_step(q, kn, vn, lg)

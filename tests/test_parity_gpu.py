@@ -14,8 +14,14 @@ from _parity import Pair, confident_logits, step_inputs
 pytestmark = pytest.mark.gpu
 
 
-def _run(w, seed, steps, prefill_len=None, confident_every=0, cap=None, check_state=True):
-    p = Pair(w, seed, prefill_len=prefill_len, cap=cap)
+# confkv_step modes: one fused launch per step where the shape allows it
+# (the default), and the three separate kernels
+MODES = [ck.binding.STEP_AUTO, ck.binding.STEP_SEPARATE]
+MODE_IDS = ["fused", "separate"]
+
+
+def _run(w, seed, steps, prefill_len=None, confident_every=0, cap=None, check_state=True, mode=0):
+    p = Pair(w, seed, prefill_len=prefill_len, cap=cap, mode=mode)
     p.compare_states()
     for s in range(steps):
         q, kn, vn, lg = step_inputs(w, seed, s)
@@ -25,27 +31,31 @@ def _run(w, seed, steps, prefill_len=None, confident_every=0, cap=None, check_st
     return p
 
 
-def test_gqa5_d128_ragged_prefills_and_flips():
+@pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
+def test_gqa5_d128_ragged_prefills_and_flips(mode):
     w = Workload(name="t_gqa", B=3, L=2, Hq=10, Hkv=2, d=128, V=3000, T0=300, steps=40,
                  n_high=(40, 30), n_low=(120, 90), P=8, W=32, q_dtype="bf16",
                  heavy_count=5, heavy_factor=3.0, logit_sigma=1.5, spike_hi=14.0)
-    p = _run(w, 11, 40, prefill_len=[300, 17, 0], confident_every=5)
+    p = _run(w, 11, 40, prefill_len=[300, 17, 0], confident_every=5, mode=mode)
     assert p.flags.evictions > 0
     assert p.flags.max_out_err <= 2e-3
+    assert p.cache.stats()["launches"] == p.launches == (40 if mode == ck.binding.STEP_AUTO else 120)
 
 
-def test_mha_d64_fp16_queries():
+@pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
+def test_mha_d64_fp16_queries(mode):
     w = Workload(name="t_mha", B=2, L=3, Hq=4, Hkv=4, d=64, V=5000, T0=200, steps=30,
                  n_high=(64,) * 3, n_low=(128,) * 3, P=16, W=64, q_dtype="f16",
                  heavy_count=3, heavy_factor=4.0)
-    p = _run(w, 12, 30, prefill_len=[200, 150], confident_every=4)
+    p = _run(w, 12, 30, prefill_len=[200, 150], confident_every=4, mode=mode)
     assert p.flags.evictions > 0
 
 
-def test_gqa8_pyramidal_budgets():
+@pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
+def test_gqa8_pyramidal_budgets(mode):
     w = Workload(name="t_g8", B=2, L=3, Hq=16, Hkv=2, d=128, V=2000, T0=160, steps=20,
                  n_high=(48, 40, 32), n_low=(96, 80, 64), P=12, W=24, q_dtype="f16")
-    p = _run(w, 13, 20, confident_every=3)
+    p = _run(w, 13, 20, confident_every=3, mode=mode)
     assert p.flags.evictions > 0
 
 
@@ -133,23 +143,25 @@ def test_full_kv_long_ring_on_the_persistent_kernel():
     assert p.flags.max_out_err <= 2e-3
 
 
-def test_sliding_window_policy_alpha_zero():
+@pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
+def test_sliding_window_policy_alpha_zero(mode):
     # recency only: alpha = 0 ranks by position, so every eviction takes the
     # oldest candidates
     w = Workload(name="t_slide", B=2, L=2, Hq=8, Hkv=2, d=64, V=800, T0=150, steps=12,
                  n_high=(64,) * 2, n_low=(64,) * 2, alpha=0.0, P=8, W=64, q_dtype="f16")
-    p = _run(w, 18, 12)
+    p = _run(w, 18, 12, mode=mode)
     assert p.flags.evictions > 0
 
 
-def test_captured_step_replays_match_the_oracle():
+@pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
+def test_captured_step_replays_match_the_oracle(mode):
     # one step captured into a CUDA graph, replayed with new inputs copied
     # into the captured buffers: the device-side step index advances, the
     # host accounts for each replay inside a reservation
     w = Workload(name="t_graph", B=2, L=2, Hq=10, Hkv=2, d=128, V=3000, T0=260, steps=12,
                  n_high=(40, 30), n_low=(100, 90), P=8, W=32, q_dtype="bf16",
                  heavy_count=5, heavy_factor=3.0)
-    p = Pair(w, 19)
+    p = Pair(w, 19, mode=mode)
     q0, kn0, vn0, lg0 = step_inputs(w, 19, 0)
     p.step(q0, kn0, vn0, lg0)                       # plain step first
     sq, skn, svn, slg = q0.cuda(), kn0.cuda(), vn0.cuda(), lg0.cuda()
@@ -213,12 +225,13 @@ def test_order_preserving_compaction_ablation():
     assert p.cache.stats()["moved"] > 0
 
 
-def test_bounded_wait_reports_a_timeout_and_the_context_survives():
+@pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
+def test_bounded_wait_reports_a_timeout_and_the_context_survives(mode):
     # failure detection without a fault: a wait that nothing satisfies runs
     # out, the status word says so, and the context keeps working
     w = Workload(name="t_to", B=1, L=1, Hq=4, Hkv=2, d=64, V=500, T0=40, steps=2,
                  n_high=(32,), n_low=(48,), P=4, W=16, q_dtype="f16")
-    p = Pair(w, 24)
+    p = Pair(w, 24, mode=mode)
     p.cache.selftest_timeout()
     st = p.cache.stats(check=False)
     assert st["device_status"] & ck.binding.STATUS_TIMEOUT
@@ -233,21 +246,24 @@ def test_bounded_wait_reports_a_timeout_and_the_context_survives():
     p.step(q, kn, vn, lg)
 
 
-def test_no_eviction_limit_is_plain_attention():
+@pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
+def test_no_eviction_limit_is_plain_attention(mode):
     # budgets above every cache length: nothing is evicted, nothing moves
     w = Workload(name="t_noop", B=2, L=2, Hq=6, Hkv=3, d=64, V=1000, T0=40, steps=12,
                  n_high=(10 ** 5,) * 2, n_low=(10 ** 5,) * 2, P=4, W=16, q_dtype="f16", cap=80)
-    p = _run(w, 15, 12)
+    p = _run(w, 15, 12, mode=mode)
     assert p.flags.evictions == 0
     st = p.cache.stats()
     assert st["evicted"] == 0 and st["moved"] == 0
     assert st["requantised"] == 2 * 2 * 12
 
 
-def test_gpt2_small_batch1_full_trajectory():
+@pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
+def test_gpt2_small_batch1_full_trajectory(mode):
     # GPT-2-small geometry, 600-token prefill, all 64 decode steps free-running
     w = get_workload("gpt2_b1")
-    p = _run(w, 1001, w.steps, check_state=False)
+    p = _run(w, 1001, w.steps, check_state=False, mode=mode)
+    assert p.cache.step_launches() == (1 if mode == ck.binding.STEP_AUTO else 3)
     p.compare_states()
     assert p.flags.steps == 64
     assert p.flags.max_out_err <= 2e-3
@@ -392,7 +408,7 @@ def test_misaligned_buffers_are_refused_before_any_launch():
     # a 16-byte-aligned view at an offset is fine
     q8 = shifted(q, 8)
     p.step(q.cpu(), kn.cpu(), vn.cpu(), lg.cpu(), gpu_step=lambda *a: p.cache.step(q8, kn, vn, lg))
-    assert p.cache.stats()["launches"] == st0["launches"] + 3
+    assert p.cache.stats()["launches"] == st0["launches"] + p.cache.step_launches()
     # the allocation-free confidence call checks its pointers the same way
     c = torch.empty(w.B + 1, dtype=torch.float32, device="cuda")
     lgs = shifted(lg, 1)
@@ -402,15 +418,16 @@ def test_misaligned_buffers_are_refused_before_any_launch():
                                        ctypes.c_void_p(c.data_ptr() + 2), stream) == ck.binding.EINVAL
 
 
-def test_footprint_counters_follow_the_oracle():
+@pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
+def test_footprint_counters_follow_the_oracle(mode):
     # resident entries and K/V bytes at stored widths, and their exact peak
     # over the steps, against the oracle's state (Pair checks every step);
     # the workspace (allocator) bytes are the context's fixed footprint
     w = Workload(name="t_foot", B=3, L=2, Hq=10, Hkv=2, d=128, V=3000, T0=300, steps=20,
                  n_high=(40, 30), n_low=(120, 90), P=8, W=32, q_dtype="bf16")
-    p = _run(w, 26, 20, prefill_len=[300, 17, 0], confident_every=4)
+    p = _run(w, 26, 20, prefill_len=[300, 17, 0], confident_every=4, mode=mode)
     st = p.cache.stats()
     assert st["peak_resident"] == p.peak_entries > 0
     assert st["peak_resident_bytes"] == p.peak_bytes > 0
     assert st["workspace_bytes"] == ck.workspace_bytes(p.cache.cfg) == p.cache.workspace.numel()
-    assert st["steps"] == 20 and st["launches"] == 60
+    assert st["steps"] == 20 and st["launches"] == p.launches == (20 if mode == ck.binding.STEP_AUTO else 60)

@@ -74,9 +74,19 @@ Shape make_shape(const confkv_config* c) {
   s.P = c->P;
   s.S = s.cap + s.WR;
   s.cstride = s.cap + 16;
-  // vocabulary chunks per sequence: 4096 logits each (16 per thread of a
-  // 256-thread block); wider vocabularies than kMaxSV chunks are rejected
-  s.SV = std::min(std::max((c->V + 4095) / 4096, 1), kMaxSV);
+  // vocabulary chunks per sequence: at most 4096 logits each (16 per thread
+  // of a 256-thread prestep block).  Shapes whose every (layer, sequence,
+  // KV head) unit can have an SM of its own (the fused step) take the
+  // smallest chunks from 512 logits up that leave at most one chunk per
+  // unit: one warp of a unit's CTA reduces a chunk while the unit streams.
+  // Wider vocabularies than kMaxSV chunks are rejected.
+  const long long units = (long long)c->L * c->B * c->Hkv;
+  int chunk = 4096;
+  if (units <= attention_persistent_ctas() / 2) {
+    chunk = 512;
+    while (chunk < 4096 && (long long)c->B * ((c->V + chunk - 1) / chunk) > units) chunk *= 2;
+  }
+  s.SV = std::min(std::max((c->V + chunk - 1) / chunk, 1), kMaxSV);
   s.qbf16 = c->q_dtype == CONFKV_Q_BF16;
   s.max_evict = c->max_evict > 0 ? c->max_evict : s.cap + s.WR;
   s.tau = c->tau; s.wH = c->w_H; s.wm = c->w_m; s.wp = c->w_p;

@@ -823,13 +823,17 @@ struct FusedArgs {
 // work, reusing the stage area): SelShared at 0, the selection's dynamic
 // layout from kFusedSelOff.
 constexpr int kFusedSelOff = 2048;
+// Shared ints before the fused step's selection list (s_misc[kFusedMiscInts]).
+constexpr int kFusedMiscInts = 24;
 static_assert(sizeof(SelShared) <= kFusedSelOff, "SelShared fits below the selection area");
 
-template <int D, bool kFlush, int kMode>
-__global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
+template <int D, bool kFlush, int kMode, int NC>
+__global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_persistent_kernel(
     Shape s, Dev d, const void* __restrict__ q, float* __restrict__ out,
     int32_t* __restrict__ budget, float* __restrict__ conf_out, const float* __restrict__ logits,
     int stages, FusedArgs fa) {
+  static_assert(NC == 4 || NC == 8, "consumer warps");
+  constexpr int NTH = (NC + 2) * 32;   // threads: NC consumer warps, the producer, the epilogue warp
   constexpr bool kFused = kMode != kModeAttention;
   constexpr bool kDevStep = kMode == kModeFusedDevStep;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -840,7 +844,7 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
   unsigned char* sbuf = smem_raw;                                          // [stages][kStageBytes]
   unsigned char* hbuf = smem_raw + (size_t)stages * kStageBytes;           // [2][hl.bytes]
   float* wpart = reinterpret_cast<float*>(hbuf + 2 * hl.bytes);            // [2][4][G][D + 2]
-  const int part_floats = kPConsumers * G * (D + 2);
+  const int part_floats = NC * G * (D + 2);
   uint64_t* bars = reinterpret_cast<uint64_t*>(wpart + 2 * part_floats);
   int* s_misc = reinterpret_cast<int*>(bars + 2 * kPMaxStages + 10);
   int& s_abort = s_misc[0];
@@ -849,8 +853,11 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
   // on done); -1 ends the CTA's work
   volatile int* s_unit = s_misc + 1;    // [2]
   volatile int* s_eunit = s_misc + 3;   // [2]
-  // fused step: the (layer, sequence) whose selection falls to this CTA, -1 if none
-  volatile int* s_sel = s_misc + 5;
+  // fused step: the (layer, sequence) groups whose selection falls to this
+  // CTA: s_nsel of them in s_sel (at most L + 1: every layer of a sequence
+  // whose confidence this CTA merged, and the group of its own unit)
+  volatile int* s_nsel = s_misc + 5;
+  volatile int* s_sel = s_misc + kFusedMiscInts;
   // fused step: the unit's Mg[8], 1 / Lg[8] for the consumer warps' share of
   // the mass loop
   float* s_mass = reinterpret_cast<float*>(s_misc + 8);
@@ -876,69 +883,21 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
   pdl_wait();
   // fused step: the step index of the new token and of the selections
   const long long fstep = kDevStep ? __ldcg(d.step_dev) : fa.step;
-  if constexpr (kFused) {
-    if ((int)blockIdx.x >= units) {
-      // ------------------------------------------------ vocabulary CTA
-      // one chunk of one sequence's logits; the CTA that completes a
-      // sequence's chunks merges its confidence and budgets, then counts one
-      // arrival on every layer of the sequence
-      const int c = (int)blockIdx.x - units;
-      const int b = c / s.SV;
-      unsigned char* vs = smem_raw + kFusedSelOff + ((fa.sm.bytes + 127) & ~127);
-      ConfAcc* red = reinterpret_cast<ConfAcc*>(vs);                          // [6]
-      int* s_list = reinterpret_cast<int*>(vs + 6 * sizeof(ConfAcc));        // [L]
-      int* s_n = s_list + s.L;                                                // [2]
-      conf_partial_block<kPThreads / 32>(s, d, logits, b, c % s.SV, red);
-      if (threadIdx.x == 0) {
-        __threadfence();
-        s_n[0] = atomicAdd(d.conf_done + b, 1u) == (unsigned)s.SV - 1u;
-        s_n[1] = 0;
-      }
-      __syncthreads();
-      if (!s_n[0]) return;
-      if (warp == 0) {
-        __threadfence();
-        conf_merge_warp(s, d, b, budget, conf_out);
-        if (lane == 0) d.conf_done[b] = 0u;   // zero again for the next launch
-      }
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        __threadfence();
-        int n = 0;
-        for (int l = 0; l < s.L; ++l) {
-          const int lb = l * s.B + b;
-          if (atomicAdd(d.arrive + lb, 1u) == (unsigned)s.Hkv) s_list[n++] = lb;
-        }
-        s_n[1] = n;
-        __threadfence();
-      }
-      __syncthreads();
-      SelShared& sh = *reinterpret_cast<SelShared*>(smem_raw);
-      for (int i = 0; i < s_n[1]; ++i) {
-        const int lb = s_list[i];
-        if (threadIdx.x == 0) d.arrive[lb] = 0u;   // every arrival of this step is in
-        select_group<D, true, kDevStep, false, kPThreads, false>(s, d, fstep, lb, fa.evicted, fa.nevict, fa.sm,
-                                                          smem_raw + kFusedSelOff, sh);
-        __syncthreads();
-      }
-      return;
-    }
-  }
   if (threadIdx.x == 0) {
     s_abort = 0;
-    s_sel[0] = -1;
+    s_nsel[0] = 0;
     for (int i = 0; i < stages; ++i) {
       mbar_init(full_bar(i), 1);
-      mbar_init(empty_bar(i), kPConsumers);
+      mbar_init(empty_bar(i), NC);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(hfull_bar(i), 1);
-      mbar_init(hempty_bar(i), kPConsumers);
-      mbar_init(done_bar(i), kPConsumers);
+      mbar_init(hempty_bar(i), NC);
+      mbar_init(done_bar(i), NC);
       mbar_init(efree_bar(i), 1);
     }
     mbar_init(mready_bar, 1);
-    mbar_init(mdone_bar, kPConsumers + 1);
+    mbar_init(mdone_bar, NC + 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
@@ -949,20 +908,32 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
   };
   auto aborted = [&](void) { return *(volatile int*)&s_abort != 0; };
 
+  // One arrival on (layer, sequence) lb; the CTA that makes the last one
+  // (Hkv unit arrivals and one confidence arrival) runs the group's
+  // selection.  (Called by several threads of the CTA: the list grows with
+  // a shared atomic.)
+  auto arrive_group = [&](int lb) {
+    if (atomicAdd(d.arrive + lb, 1u) == (unsigned)s.Hkv) s_sel[atomicAdd((int*)s_nsel, 1)] = lb;
+  };
+
   // End of this CTA's work: in a fused step, every warp meets here once its
-  // role is done, and if this CTA made the last arrival of a (layer,
-  // sequence) the whole CTA runs that group's selection over the stage
-  // area (every bulk copy into it has landed: the producer waited for them).
+  // role is done, and the whole CTA runs the selections that fell to it over
+  // the stage area (every bulk copy into it has landed: the producer waited
+  // for them).
   auto finish = [&](void) {
     if constexpr (kFused) {
       __syncthreads();
-      const int lb = s_sel[0];
-      if (lb >= 0 && !aborted()) {
+      const int n = s_nsel[0];
+      if (n > 0 && !aborted()) {
         __threadfence();
-        if (threadIdx.x == 0) d.arrive[lb] = 0u;   // every arrival of this step is in
         SelShared& sh = *reinterpret_cast<SelShared*>(smem_raw);
-        select_group<D, true, kDevStep, false, kPThreads, false>(s, d, fstep, lb, fa.evicted, fa.nevict, fa.sm,
-                                                          smem_raw + kFusedSelOff, sh);
+        for (int i = 0; i < n; ++i) {
+          const int lb = s_sel[i];
+          if (threadIdx.x == 0) d.arrive[lb] = 0u;   // every arrival of this step is in
+          select_group<D, true, kDevStep, false, NTH, false>(s, d, fstep, lb, fa.evicted, fa.nevict, fa.sm,
+                                                            smem_raw + kFusedSelOff, sh);
+          __syncthreads();
+        }
       }
     }
   };
@@ -999,19 +970,78 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
     }
   };
 
-  if (warp == kPConsumers) {
+  if (warp == NC) {
     // ------------------------------------------------ producer warp
     if constexpr (kFused) {
-      // the new token of this CTA's unit goes to its ring slot before the
-      // unit's header and blocks are read; the proxy fence orders these
-      // stores before the bulk copies (async proxy) that read them back
-      if ((int)blockIdx.x < units) {
-        const int u = blockIdx.x;
-        const int b = (u / s.Hkv) % s.B;
-        append_unit_warp<D>(s, d, u, d.T0[b] + (int)fstep, fa.k_new, fa.v_new);
+      // Fused step: this CTA's one unit, u = blockIdx.x.  The header (q and
+      // the scales) and the INT8 blocks do not depend on this step's new
+      // token, so their bulk copies go first; then the whole warp appends
+      // the new token to its ring slot, and the proxy fence orders those
+      // stores before the ring blocks' bulk copies (async proxy) read them
+      // back.  The consumers read the ring positions from global memory
+      // (after the ring stage's barrier), not from the header.
+      const uint64_t pol = policy_evict_first();
+      const int u = blockIdx.x;
+      const int h = u % s.Hkv, b = (u / s.Hkv) % s.B, l = u / (s.Hkv * s.B);
+      const size_t lb = lb_index(s, l, b);
+      const int nb8 = (d.n8[lb] + 15) >> 4;
+      Sched sch;
+      sch.init(0, nb8 + nbR, nb8);
+      const char* k8u = reinterpret_cast<const char*>(d.k8) + (size_t)u * s.cstride * D;
+      const char* v8u = reinterpret_cast<const char*>(d.v8) + (size_t)u * s.cstride * D;
+      const char* k16u = reinterpret_cast<const char*>(d.k16) + (size_t)u * s.WR * D * 2;
+      const char* v16u = reinterpret_cast<const char*>(d.v16) + (size_t)u * s.WR * D * 2;
+      RingPos st;
+      int issued = 0;
+      bool ok = true;
+      auto issue = [&](int i) {
+        if (issued >= stages && !mbar_wait(empty_bar(st.slot), st.phase ^ 1u)) return false;
+        bool ring;
+        int first, nb;
+        sch.first_last(i, ring, first, nb);
+        const uint32_t span = (uint32_t)(nb * 16 * D * (ring ? 2 : 1));
+        const char* ksrc = ring ? k16u + (size_t)first * 32 * D : k8u + (size_t)first * 16 * D;
+        const char* vsrc = ring ? v16u + (size_t)first * 32 * D : v8u + (size_t)first * 16 * D;
+        const uint32_t dst = smem_u32(sbuf + (size_t)st.slot * kStageBytes);
+        mbar_arrive_tx(full_bar(st.slot), 2 * span);
+        bulk_g2s_hint(dst, ksrc, span, full_bar(st.slot), pol);
+        bulk_g2s_hint(dst + kHalf, vsrc, span, full_bar(st.slot), pol);
+        st.next(stages);
+        ++issued;
+        return true;
+      };
+      if (lane == 0) {
+        s_unit[0] = u;
+        const uint32_t hdst = smem_u32(hbuf);
+        const uint32_t qbytes = (uint32_t)(G * D * 2);
+        mbar_arrive_tx(hfull_bar(0), qbytes + 2u * D * 4);
+        bulk_g2s(hdst + hl.q, reinterpret_cast<const char*>(q) + (lb * s.Hq + (size_t)h * G) * D * 2, qbytes,
+                 hfull_bar(0));
+        bulk_g2s(hdst + hl.sk, d.sK + (size_t)u * D, D * 4, hfull_bar(0));
+        bulk_g2s(hdst + hl.sv, d.sV + (size_t)u * D, D * 4, hfull_bar(0));
+        for (int i = 0; i < sch.n8st && ok; ++i) ok = issue(i);
       }
+      append_unit_warp<D>(s, d, u, d.T0[b] + (int)fstep, fa.k_new, fa.v_new);
       asm volatile("fence.proxy.async.global;\n" ::: "memory");
       __syncwarp();
+      if (lane == 0) {
+        for (int i = sch.n8st; i < sch.nst && ok; ++i) ok = issue(i);
+        if (!ok) fail();
+        // no second unit: the other warps see -1 in header slot 1
+        s_unit[1] = -1;
+        mbar_arrive(hfull_bar(1));
+      }
+      if (lane == 0) {
+        // wait (bounded) for the last copy of every stage slot
+        RingPos dr = st;
+        for (int i = 0; i < stages && i < issued; ++i) {
+          dr.slot = dr.slot == 0 ? stages - 1 : dr.slot - 1;
+          if (dr.slot == stages - 1) dr.phase ^= 1u;
+          if (!mbar_wait(full_bar(dr.slot), dr.phase)) atomicOr(d.status, kStatusTimeout);
+        }
+      }
+      finish();
+      return;
     }
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
@@ -1083,10 +1113,39 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
     return;
   }
 
-  if (warp == kPConsumers + 1) {
+  if (warp == NC + 1) {
     // ------------------------------------------------ epilogue warp
     // Idle until the first unit is done: the confidence of the step.
-    if (!kFused && logits) {
+    if (kFused) {
+      // Fused step: this warp reduces CTA c's vocabulary chunk (c < B * SV,
+      // at most one per CTA) while the consumer warps stream the unit.  The
+      // CTA that completes a sequence's chunks merges its confidence and
+      // budgets and counts one arrival on every layer of the sequence (one
+      // lane per layer).  Chunks are small (512 logits), so this comes before
+      // the units finish, and the last arrival of a group, with its
+      // selection, falls to the CTA of one of its units.
+      const int c = blockIdx.x;
+      if (c < s.B * s.SV) {
+        const int bc = c / s.SV;
+        conf_partial_warp(s, d, logits, bc, c % s.SV);
+        unsigned int prev = 0;
+        if (lane == 0) {
+          __threadfence();
+          prev = atomicAdd(d.conf_done + bc, 1u);
+        }
+        prev = __shfl_sync(0xffffffffu, prev, 0);
+        if (prev == (unsigned int)s.SV - 1u) {
+          __threadfence();
+          conf_merge_warp(s, d, bc, budget, conf_out);
+          if (lane == 0) {
+            d.conf_done[bc] = 0u;   // zero again for the next launch
+            __threadfence();
+          }
+          __syncwarp();
+          for (int ll = lane; ll < s.L; ll += 32) arrive_group(ll * s.B + bc);
+        }
+      }
+    } else if (logits) {
       // Logits in host memory: this CTA reduces its vocabulary chunks to
       // partials here, so that their transfer overlaps the attention; the
       // CTA that finishes the last chunk of a sequence merges that sequence.
@@ -1121,16 +1180,16 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
       const size_t lb = lb_index(s, l, b);
       const int nb8 = (d.n8[lb] + 15) >> 4;
       const float* part = wpart + (size_t)ps * part_floats;   // [4][G][D + 2]: o..., m, l
-      float Mg[kMaxG], Lg[kMaxG], fw[kPConsumers][kMaxG];
+      float Mg[kMaxG], Lg[kMaxG], fw[NC][kMaxG];
 #pragma unroll
       for (int gg = 0; gg < kMaxG; ++gg) {
         Mg[gg] = -INFINITY;
         Lg[gg] = 0.f;
         if (gg < G) {
 #pragma unroll
-          for (int w = 0; w < kPConsumers; ++w) Mg[gg] = fmaxf(Mg[gg], part[(w * G + gg) * (D + 2) + D]);
+          for (int w = 0; w < NC; ++w) Mg[gg] = fmaxf(Mg[gg], part[(w * G + gg) * (D + 2) + D]);
 #pragma unroll
-          for (int w = 0; w < kPConsumers; ++w) {
+          for (int w = 0; w < NC; ++w) {
             const float mw = part[(w * G + gg) * (D + 2) + D];
             fw[w][gg] = (mw == -INFINITY) ? 0.f : ex2(mw - Mg[gg]);
             Lg[gg] += part[(w * G + gg) * (D + 2) + D + 1] * fw[w][gg];
@@ -1146,7 +1205,7 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
           for (int c = lane; c < D; c += 32) {
             float acc = 0.f;
 #pragma unroll
-            for (int w = 0; w < kPConsumers; ++w) acc += part[(w * G + gg) * (D + 2) + c] * fw[w][gg];
+            for (int w = 0; w < NC; ++w) acc += part[(w * G + gg) * (D + 2) + c] * fw[w][gg];
             o[gg * D + c] = acc * inv;
           }
         }
@@ -1168,13 +1227,14 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
           }
           mbar_arrive(mready_bar);
         }
-        mass_quads(u, nb8, scg, Mg, invL, kPConsumers * 32 + lane, (kPConsumers + 1) * 32);
+        mass_quads(u, nb8, scg, Mg, invL, NC * 32 + lane, (NC + 1) * 32);
         __threadfence();
         __syncwarp();
         if (lane == 0) mbar_arrive(mdone_bar);
+        // every share's stores were made visible by its own warp's fence
+        // before that warp arrived
         if (!mbar_wait(mdone_bar, 0)) fail();
-        __threadfence();
-        if (lane == 0 && !aborted() && atomicAdd(d.arrive + lb, 1u) == (unsigned)s.Hkv) s_sel[0] = (int)lb;
+        if (lane == 0 && !aborted()) arrive_group((int)lb);
       } else {
         mass_quads(u, nb8, scg, Mg, invL, lane, 32);
       }
@@ -1214,8 +1274,8 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
     const unsigned char* hdr = hbuf + (size_t)hs * hl.bytes;
     const float* sKh = reinterpret_cast<const float*>(hdr + hl.sk);
     const float* sVh = reinterpret_cast<const float*>(hdr + hl.sv);
-    const int32_t* posh = hl.pos_in ? reinterpret_cast<const int32_t*>(hdr + hl.pos)
-                                    : d.pos + lb * s.S + s.cap;
+    const int32_t* posh = (hl.pos_in && !kFused) ? reinterpret_cast<const int32_t*>(hdr + hl.pos)
+                                                 : d.pos + lb * s.S + s.cap;
     float* scg = scg_base + (size_t)hs * G * s.S;
     Sched sch;
     sch.init(0, nb8 + nbR, nb8);
@@ -1238,16 +1298,19 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
       const uint32_t stage = smem_u32(sbuf + (size_t)st.slot * kStageBytes);
       int tok0 = -1;
       if (!ring) {
-        if (warp < nb) {
-          const int blk = first + warp;
+        // an INT8 stage holds 4 blocks: with 8 consumer warps, warps 0-3 take
+        // the even INT8 stages and warps 4-7 the odd ones
+        const int wi = warp & 3;
+        if ((warp >> 2) == i % (NC / 4) && wi < nb) {
+          const int blk = first + wi;
           tok0 = blk * 16;
-          int8_block<D, kFlush>(ws, stage + warp * 16 * D, stage + kHalf + warp * 16 * D, blk, n8, G, g,
+          int8_block<D, kFlush>(ws, stage + wi * 16 * D, stage + kHalf + wi * 16 * D, blk, n8, G, g,
                                 t, lane, nullptr, sc4buf);
         }
       } else {
-        // a ring stage holds 2 FP16 blocks: warps 0-1 take the even ring
-        // stages, warps 2-3 the odd ones, so both pairs work at once
-        const int jb = warp - 2 * ((i - sch.n8st) & 1);
+        // a ring stage holds 2 FP16 blocks: the warp pairs (0-1, 2-3, ...)
+        // take the ring stages in turn, so every pair works at once
+        const int jb = warp - 2 * ((i - sch.n8st) % (NC / 2));
         if (jb >= 0 && jb < nb) {
           if (!ws.in_ring) {
             make_q_frag_s<D>(ws.aq, hdr + hl.q, s.qbf16, nullptr, qs, G, g, t);
@@ -1314,7 +1377,7 @@ __global__ void __launch_bounds__(kPThreads, 2) attention_persistent_kernel(
           invL[gg] = s_mass[kMaxG + gg];
         }
         const int nb8 = (d.n8[u0 / s.Hkv] + 15) >> 4;
-        mass_quads(u0, nb8, scg_base, Mg, invL, (int)threadIdx.x, (kPConsumers + 1) * 32);
+        mass_quads(u0, nb8, scg_base, Mg, invL, (int)threadIdx.x, (NC + 1) * 32);
         __threadfence();
         __syncwarp();
         if (lane == 0) mbar_arrive(mdone_bar);
@@ -1344,10 +1407,16 @@ static int fixed_bytes_split(const Shape& s, int splits, int max_tokens) {
   return (int)(f * sizeof(float)) + 2 * kMaxStages * 8;
 }
 
-static int fixed_bytes_persistent(const Shape& s) {
+// Fused steps run the persistent kernel with 8 consumer warps, one CTA per
+// SM (every unit on an SM of its own); the attention-only launch with 4,
+// two CTAs per SM.
+constexpr int kFusedConsumers = 8;
+
+static int fixed_bytes_persistent(const Shape& s, int nc = kPConsumers) {
   const HeaderLayout hl(s.G, s.D, s.WR);
-  const int part = kPConsumers * s.G * (s.D + 2) * 4;
-  return 2 * hl.bytes + 2 * part + (2 * kPMaxStages + 10) * 8 + 96;
+  const int part = nc * s.G * (s.D + 2) * 4;
+  const int misc = ((kFusedMiscInts + s.L + 2) * 4 + 15) / 16 * 16;
+  return 2 * hl.bytes + 2 * part + (2 * kPMaxStages + 10) * 8 + misc;
 }
 
 int attention_max_smem() { return 225 * 1024; }
@@ -1358,9 +1427,11 @@ static int stages_split(const Shape& s, int splits, int max_tokens) {
   return st > kMaxStages ? kMaxStages : (st < 2 ? 2 : st);
 }
 
-// Persistent kernel: as many stages as fit while two CTAs share an SM.
-static int stages_persistent(const Shape& s) {
-  int st = (113 * 1024 - fixed_bytes_persistent(s)) / stage_bytes(s.D);
+// Persistent kernel: as many stages as fit while two CTAs share an SM (4
+// consumer warps), or in the whole SM (8).
+static int stages_persistent(const Shape& s, int nc = kPConsumers) {
+  const int budget = nc == kPConsumers ? 113 * 1024 : 225 * 1024;
+  int st = (budget - fixed_bytes_persistent(s, nc)) / stage_bytes(s.D);
   return st > kPMaxStages ? kPMaxStages : (st < 2 ? 2 : st);
 }
 
@@ -1451,8 +1522,8 @@ static int launch_d(const Shape& s, const Dev& d, const void* q, float* out, int
     // at its register limit (0.292 against 0.285 ms on the Qwen-32B shape).
     static int configured[2][kMaxDevices] = {};
     const bool flush = max_tokens - s.WR > kFlushTokens;
-    auto kern = flush ? attention_persistent_kernel<D, true, kModeAttention>
-                      : attention_persistent_kernel<D, false, kModeAttention>;
+    auto kern = flush ? attention_persistent_kernel<D, true, kModeAttention, kPConsumers>
+                      : attention_persistent_kernel<D, false, kModeAttention, kPConsumers>;
     if (ensure_smem(kern, attention_max_smem(), configured[flush]) != cudaSuccess) return -1;
     int grid = 0, cluster = 0;
     attention_grid(s, d, 1, &grid, &cluster);
@@ -1480,22 +1551,24 @@ static int launch_d(const Shape& s, const Dev& d, const void* q, float* out, int
   return e == cudaSuccess ? 0 : -1;
 }
 
-// A fused step: every unit on a CTA of its own next to one CTA per
-// vocabulary chunk, all in one wave of the persistent grid; units short
-// enough for the instance without the INT8 V bias flush; tail-fill
-// compaction; and the selection's keys and bitmaps inside the stage area.
+// A fused step: every unit on a CTA of its own and one CTA per SM (8
+// consumer warps), at most one vocabulary chunk per CTA; units short enough
+// for the instance without the INT8 V bias flush; tail-fill compaction; and
+// the selection's keys and bitmaps inside the stage area.
 bool fused_step_fits(const Shape& s, const Dev& d, int splits, int max_tokens) {
   const long long units = (long long)s.L * s.B * s.Hkv;
   if (splits != 1 || s.compaction != 0) return false;
-  if (units + (long long)s.B * s.SV > attention_persistent_ctas()) return false;
-  if (d.attn_ctas > 0 && units + (long long)s.B * s.SV > d.attn_ctas) return false;
+  if (units > attention_persistent_ctas() / 2) return false;
+  // each CTA's epilogue warp reduces at most one vocabulary chunk, so it
+  // merges at most one sequence (its selection list holds L + 1 groups)
+  if ((long long)s.B * s.SV > units) return false;
+  if (d.attn_ctas > 0 && units > d.attn_ctas) return false;
   if (units > d.score_ctas) return false;
   if (max_tokens - s.WR > kFlushTokens) return false;
   const SelSmem sm = plan_select(s);
   if (sm.off_key < 0) return false;
-  const long long need = kFusedSelOff + ((sm.bytes + 127) & ~127) + 6 * (long long)sizeof(ConfAcc) +
-                         4LL * (s.L + 2);
-  return need <= (long long)stages_persistent(s) * stage_bytes(s.D);
+  const long long need = kFusedSelOff + ((sm.bytes + 127) & ~127);
+  return need <= (long long)stages_persistent(s, kFusedConsumers) * stage_bytes(s.D);
 }
 
 template <int D>
@@ -1504,11 +1577,12 @@ static int launch_fused_d(const Shape& s, const Dev& d, long long step, const vo
                           int32_t* evicted_pos, int32_t* n_evicted, cudaStream_t stream) {
   static int configured[2][kMaxDevices] = {};
   const bool dev = step < 0;
-  auto kern = dev ? attention_persistent_kernel<D, false, kModeFusedDevStep>
-                  : attention_persistent_kernel<D, false, kModeFused>;
+  auto kern = dev ? attention_persistent_kernel<D, false, kModeFusedDevStep, kFusedConsumers>
+                  : attention_persistent_kernel<D, false, kModeFused, kFusedConsumers>;
   if (ensure_smem(kern, attention_max_smem(), configured[dev]) != cudaSuccess) return -1;
-  const int smem = stages_persistent(s) * stage_bytes(D) + fixed_bytes_persistent(s);
-  const int grid = s.L * s.B * s.Hkv + s.B * s.SV;
+  const int stages = stages_persistent(s, kFusedConsumers);
+  const int smem = stages * stage_bytes(D) + fixed_bytes_persistent(s, kFusedConsumers);
+  const int grid = s.L * s.B * s.Hkv;
   FusedArgs fa{};
   fa.step = step;
   fa.k_new = static_cast<const __half*>(k_new);
@@ -1516,8 +1590,8 @@ static int launch_fused_d(const Shape& s, const Dev& d, long long step, const vo
   fa.evicted = evicted_pos;
   fa.nevict = n_evicted;
   fa.sm = plan_select(s);
-  return launch_pdl(kern, dim3(grid), dim3(kPThreads), (size_t)smem, stream, s, d, q, out, budget, conf_out,
-                    logits, stages_persistent(s), fa) == cudaSuccess
+  return launch_pdl(kern, dim3(grid), dim3((kFusedConsumers + 2) * 32), (size_t)smem, stream, s, d, q, out,
+                    budget, conf_out, logits, stages, fa) == cudaSuccess
              ? 0
              : -1;
 }

@@ -134,100 +134,6 @@ __device__ __forceinline__ void conf_partial_warp(const Shape& s, const Dev& d,
   }
 }
 
-// One warp's share [v0, v1) of a vocabulary chunk of row z, reduced to the
-// chunk partial's fields (every lane returns the warp's values, relative to
-// the warp maximum M).  Same single pass as conf_partial_warp.
-struct ConfAcc {
-  float M;
-  FSum S, T;
-  Top2 tp;
-};
-
-__device__ __forceinline__ ConfAcc conf_range_warp(const float* __restrict__ z, int v0, int v1) {
-  constexpr int kIn = 8;   // loads in flight per lane
-  const int lane = threadIdx.x & 31;
-  float m = -FLT_MAX;
-  FSum S{0.f, 0.f}, T{0.f, 0.f};
-  Top2 tp{-FLT_MAX, -FLT_MAX, 0x7fffffff};
-  for (int base = v0; base < v1; base += 32 * kIn) {
-    float x[kIn];
-#pragma unroll
-    for (int j = 0; j < kIn; ++j) {
-      const int idx = base + 32 * j + lane;
-      x[j] = idx < v1 ? __ldg(z + idx) : -FLT_MAX;
-    }
-#pragma unroll
-    for (int j = 0; j < kIn; ++j) {
-      const int idx = base + 32 * j + lane;
-      if (idx < v1) {
-        if (x[j] > m) {
-          conf_rescale(S, T, m, x[j]);
-          m = x[j];
-        }
-        const float dz = x[j] - m;
-        const float e = expf(dz);
-        S = fsum_add(S, e);
-        T = fsum_add(T, dz * e);
-        tp = top2_merge(tp, Top2{x[j], -FLT_MAX, idx});
-      }
-    }
-  }
-  float M = m;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  conf_rescale(S, T, m, M);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    S = fsum_add(S, fsum_shfl_xor(S, o));
-    T = fsum_add(T, fsum_shfl_xor(T, o));
-    Top2 other{__shfl_xor_sync(0xffffffffu, tp.z1, o), __shfl_xor_sync(0xffffffffu, tp.z2, o),
-               __shfl_xor_sync(0xffffffffu, tp.i1, o)};
-    tp = top2_merge(tp, other);
-  }
-  return ConfAcc{M, S, T, tp};
-}
-
-// Partial of vocabulary chunk `part` of sequence b computed by a whole block
-// of NW warps: each warp reduces a contiguous share of the chunk, then
-// thread 0 brings the warps' sums to the chunk maximum and adds them.
-// `red` holds NW ConfAcc in shared memory.  Called by every thread.
-template <int NW>
-__device__ __forceinline__ void conf_partial_block(const Shape& s, const Dev& d, const float* __restrict__ logits,
-                                                   int b, int part, ConfAcc* red) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int V = s.V;
-  const int chunk = (V + s.SV - 1) / s.SV;
-  const int v0 = part * chunk, v1 = min(V, v0 + chunk);
-  const int share = ((max(v1 - v0, 0) + NW - 1) / NW + 31) / 32 * 32;
-  const int w0 = min(v1, v0 + warp * share), w1 = min(v1, w0 + share);
-  const ConfAcc a = conf_range_warp(logits + (size_t)b * V, w0, w1);
-  if (lane == 0) red[warp] = a;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float M = -FLT_MAX;
-    for (int w = 0; w < NW; ++w) M = fmaxf(M, red[w].M);
-    FSum S{0.f, 0.f}, T{0.f, 0.f};
-    Top2 tp{-FLT_MAX, -FLT_MAX, 0x7fffffff};
-    for (int w = 0; w < NW; ++w) {
-      FSum Sw = red[w].S, Tw = red[w].T;
-      conf_rescale(Sw, Tw, red[w].M, M);
-      S = fsum_add(S, Sw);
-      T = fsum_add(T, Tw);
-      tp = top2_merge(tp, red[w].tp);
-    }
-    ConfPartial cp;
-    cp.M = (v1 > v0) ? M : -FLT_MAX;
-    cp.z1 = tp.z1;
-    cp.z2 = tp.z2;
-    cp.i1 = tp.i1;
-    cp.S = S.hi;
-    cp.Se = S.lo;
-    cp.T = T.hi;
-    cp.Te = T.lo;
-    d.conf[(size_t)b * s.SV + part] = cp;
-  }
-}
-
 static_assert(sizeof(ConfPartial) == 32, "ConfPartial is read as two 16-byte words");
 
 // One chunk partial read from L2 (written by other CTAs of the same kernel
@@ -249,28 +155,51 @@ __device__ __forceinline__ ConfPartial load_partial(const ConfPartial* p) {
 
 // c of one sequence from its SV chunk partials cp[0 .. SV) over a vocabulary
 // of V, with the weights (wH, wm, wp).  Called by all 32 lanes of one warp;
-// every lane returns c.
+// every lane returns c.  One pass: each lane folds its partials into a
+// running (M, S, T) with the same rescaling as the single-chunk pass, four
+// partials loaded at a time; then the lanes are brought to the common
+// maximum and summed.
 __device__ __forceinline__ float conf_merge_c(const ConfPartial* __restrict__ cp, int SV, int V,
                                               float wH, float wm, float wp) {
   const int lane = threadIdx.x & 31;
-  float M = -FLT_MAX;
-  for (int i = lane; i < SV; i += 32) M = fmaxf(M, __ldcg(&cp[i].M));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float m = -FLT_MAX;
   FSum S{0.f, 0.f}, T{0.f, 0.f};
   Top2 tp{-FLT_MAX, -FLT_MAX, 0x7fffffff};
-  for (int i = lane; i < SV; i += 32) {
-    const ConfPartial p = load_partial(cp + i);
-    if (p.M > -FLT_MAX) {
-      const float dm = p.M - M;
-      const float f = expf(dm);
-      S = fsum_add(S, p.S * f);
-      S = fsum_add(S, p.Se * f);
-      T = fsum_add(T, (p.T + dm * p.S) * f);
-      T = fsum_add(T, (p.Te + dm * p.Se) * f);
+  for (int i0 = lane; i0 < SV; i0 += 32 * 4) {
+    ConfPartial p[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = i0 + 32 * j;
+      if (i < SV) {
+        p[j] = load_partial(cp + i);
+      } else {
+        p[j].M = -FLT_MAX;
+        p[j].z1 = p[j].z2 = -FLT_MAX;
+        p[j].i1 = 0x7fffffff;
+        p[j].S = p[j].Se = p[j].T = p[j].Te = 0.f;
+      }
     }
-    tp = top2_merge(tp, Top2{p.z1, p.z2, p.i1});
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (p[j].M > -FLT_MAX) {
+        if (p[j].M > m) {
+          conf_rescale(S, T, m, p[j].M);
+          m = p[j].M;
+        }
+        const float dm = p[j].M - m;
+        const float f = expf(dm);
+        S = fsum_add(S, p[j].S * f);
+        S = fsum_add(S, p[j].Se * f);
+        T = fsum_add(T, (p[j].T + dm * p[j].S) * f);
+        T = fsum_add(T, (p[j].Te + dm * p[j].Se) * f);
+      }
+      tp = top2_merge(tp, Top2{p[j].z1, p[j].z2, p[j].i1});
+    }
   }
+  float M = m;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  conf_rescale(S, T, m, M);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     S = fsum_add(S, fsum_shfl_xor(S, o));
@@ -282,9 +211,9 @@ __device__ __forceinline__ float conf_merge_c(const ConfPartial* __restrict__ cp
   const float Sv = S.hi + S.lo, Tv = T.hi + T.lo;
   const float H = logf(Sv) - Tv / Sv;
   const float Hhat = H / logf((float)V);
-  const float m = tp.z1 - tp.z2;
+  const float mg = tp.z1 - tp.z2;
   const float p1 = expf(tp.z1 - M) / Sv;
-  return wH * (1.0f - Hhat) + wm * (1.0f / (1.0f + expf(-m))) + wp * p1;
+  return wH * (1.0f - Hhat) + wm * (1.0f / (1.0f + expf(-mg))) + wp * p1;
 }
 
 // Merges the partials of sequence b and publishes c (d.cval, conf_out) and

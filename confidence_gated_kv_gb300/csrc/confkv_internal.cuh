@@ -280,7 +280,9 @@ int launch_select(const Shape& s, const Dev& d, long long step, int32_t* evicted
 int attention_smem_bytes(const Shape& s, int splits, int max_tokens);
 // Fused step: one launch for the whole decode step (append, vocabulary
 // reduction and confidence, attention with mass, and every selection) when
-// fused_step_fits; step as for launch_prestep.
+// fused_step_fits: one CTA per unit and per SM, each CTA's epilogue warp
+// reducing a vocabulary chunk while the unit streams; step as for
+// launch_prestep.
 bool fused_step_fits(const Shape& s, const Dev& d, int splits, int max_tokens);
 int launch_fused_step(const Shape& s, const Dev& d, long long step, const void* q, const void* k_new,
                       const void* v_new, const float* logits, float* out, int32_t* budget, float* conf_out,

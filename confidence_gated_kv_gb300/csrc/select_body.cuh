@@ -44,7 +44,7 @@ namespace confkv {
 
 constexpr int kSelThreads = 256;           // threads of the select kernel
 constexpr int kSelWarps = kSelThreads / 32;
-constexpr int kSelMaxWarps = 8;            // warps of any block that runs select_group
+constexpr int kSelMaxWarps = 10;           // warps of any block that runs select_group
 constexpr int kPosWords = 2048;            // sorted-output bitmap: 65536 positions per window
 constexpr uint32_t kNoKey = 0xffffffffu;   // ranking key of a slot that is not a candidate
 constexpr size_t kSelSmemKeysMax = 100 * 1024;
@@ -69,7 +69,7 @@ struct SelShared {
   unsigned long long red64[kSelMaxWarps];
   int hist[256];
   int scan_w[kSelMaxWarps];
-  int s_digit, s_rem, s_dcnt, s_cnt, s_k8, s_evslot, s_evpos;
+  int s_digit, s_rem, s_dcnt, s_cnt, s_k8, s_evslot, s_evpos, s_prs;
 };
 
 // Order-preserving compaction of the INT8 region (the ablation of tail fill):
@@ -213,7 +213,7 @@ __device__ __forceinline__ void hist_find(const int* hist, int rem, int lane, in
 }
 
 // The selection of one (layer, sequence) lb = l * B + b, run by a whole
-// block of NT threads (a multiple of 32, at most 256): the EMA update, the
+// block of NT threads (a multiple of 32, at most 320): the EMA update, the
 // ranking and bottom-k, the sorted evicted positions, compaction and
 // requantisation.  dsm is dynamic shared memory laid out as `sm` describes,
 // sh the small shared arrays; the caller's block synchronises before and
@@ -227,7 +227,7 @@ template <int D, bool kSmemKeys, bool kDevStep, bool kOrdered, int NT, bool kGri
 __device__ __forceinline__ void select_group(const Shape s, const Dev d, long long step_arg, int lbi_arg,
                                              int32_t* __restrict__ evicted_out, int32_t* __restrict__ nevict_out,
                                              const SelSmem sm, unsigned char* dsm, SelShared& sh) {
-  static_assert(NT % 32 == 0 && NT / 32 <= kSelMaxWarps && NT <= 256, "select_group block size");
+  static_assert(NT % 32 == 0 && NT / 32 <= kSelMaxWarps, "select_group block size");
   constexpr int NW = NT / 32;
   uint32_t* posbits = reinterpret_cast<uint32_t*>(dsm + sm.off_posbits);
   uint32_t* bm8 = reinterpret_cast<uint32_t*>(dsm + sm.off_bm8);
@@ -243,6 +243,7 @@ __device__ __forceinline__ void select_group(const Shape s, const Dev d, long lo
   int& s_k8 = sh.s_k8;
   int& s_evslot = sh.s_evslot;
   int& s_evpos = sh.s_evpos;
+  int& s_prs = sh.s_prs;
 
   // a step inside a graph reservation reads the step index from the device
   const long long step = kDevStep ? __ldcg(d.step_dev) : step_arg;
@@ -262,7 +263,6 @@ __device__ __forceinline__ void select_group(const Shape s, const Dev d, long lo
   const int tl = t - s.W;                  // position leaving the FP16 window
   const int rs = tl >= 0 ? tl % WR : 0;
   const int rslot = cap + rs;
-  const int prs = tl >= 0 ? pos[rslot] : -1;   // read before any slot of this step changes
   const int nvirt = n8 + WR;               // element e: INT8 slot e < n8, else ring slot cap + e - n8
   auto slot_of = [&](int e) { return e < n8 ? e : cap + (e - n8); };
 
@@ -297,67 +297,96 @@ __device__ __forceinline__ void select_group(const Shape s, const Dev d, long lo
   int nring = 0, ncand = 0;
   float amin = FLT_MAX, amax = -FLT_MAX;
   int pmin = INT_MAX, pmax = INT_MIN;
-  for (int q0 = threadIdx.x; q0 < nq; q0 += 2 * NT) {
-    int4 P4[2];
-    float4 E4[2], A4[2];
+  // One quad of slots: the EMA update, the ranking's candidate ranges, the
+  // keys in shared memory; the position held by the slot whose token leaves
+  // the FP16 window (read here, before any slot of this step changes).
+  auto ema_quad = [&](int q, const int4 P4, const float4 E4, const float4 A4) {
+    const bool ring = q >= q8;
+    const int slot0 = ring ? cap + 4 * (q - q8) : 4 * q;
+    const int pv[4] = {P4.x, P4.y, P4.z, P4.w};
+    const float ev[4] = {E4.x, E4.y, E4.z, E4.w};
+    const float av[4] = {A4.x, A4.y, A4.z, A4.w};
+    float nv[4];
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int q = q0 + r * NT;
-      P4[r] = make_int4(-1, -1, -1, -1);
-      E4[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-      A4[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (q < nq) {
-        const int slot0 = q < q8 ? 4 * q : cap + 4 * (q - q8);
-        P4[r] = *reinterpret_cast<const int4*>(pos + slot0);
-        E4[r] = *reinterpret_cast<const float4*>(ema + slot0);
+    for (int j = 0; j < 4; ++j) {
+      const int p = pv[j];
+      const bool valid = ring ? p >= 0 : 4 * q + j < n8;
+      nv[j] = ev[j];
+      int cp = INT_MAX;
+      if (valid) {
+        const float a = fmaf(lam, ev[j], (1.0f - lam) * (av[j] * inv_hq));
+        nv[j] = a;
+        nring += ring;
+        if (p < thr) {
+          cp = p;
+          ++ncand;
+          amin = fminf(amin, a); amax = fmaxf(amax, a);
+          pmin = min(pmin, p); pmax = max(pmax, p);
+        }
       }
+      if (kSmemKeys) {
+        KEY[slot0 + j] = __float_as_uint(nv[j]);
+        SPOS[slot0 + j] = cp;
+      }
+      // (rslot lies in exactly one ring quad; s_prs is read only when tl >= 0)
+      if (ring && tl >= 0 && slot0 + j == rslot) s_prs = p;
     }
-#pragma unroll 4
-    for (int h = 0; h < Hkv; ++h) {
+    *reinterpret_cast<float4*>(ema + slot0) = make_float4(nv[0], nv[1], nv[2], nv[3]);
+  };
+  if constexpr (kGrid) {
+    // two quads per thread and pass (a long cache over 256 threads)
+    for (int q0 = threadIdx.x; q0 < nq; q0 += 2 * NT) {
+      int4 P4[2];
+      float4 E4[2], A4[2];
 #pragma unroll
       for (int r = 0; r < 2; ++r) {
         const int q = q0 + r * NT;
+        P4[r] = make_int4(-1, -1, -1, -1);
+        E4[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+        A4[r] = make_float4(0.f, 0.f, 0.f, 0.f);
         if (q < nq) {
           const int slot0 = q < q8 ? 4 * q : cap + 4 * (q - q8);
-          const float4* mp = reinterpret_cast<const float4*>(mass + (size_t)h * S + slot0);
-          const float4 m = kGrid ? __ldg(mp) : __ldcg(mp);
-          A4[r].x += m.x; A4[r].y += m.y; A4[r].z += m.z; A4[r].w += m.w;
+          P4[r] = *reinterpret_cast<const int4*>(pos + slot0);
+          E4[r] = *reinterpret_cast<const float4*>(ema + slot0);
         }
       }
-    }
+#pragma unroll 4
+      for (int h = 0; h < Hkv; ++h) {
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int q = q0 + r * NT;
-      if (q >= nq) continue;
-      const bool ring = q >= q8;
-      const int slot0 = ring ? cap + 4 * (q - q8) : 4 * q;
-      const int pv[4] = {P4[r].x, P4[r].y, P4[r].z, P4[r].w};
-      const float ev[4] = {E4[r].x, E4[r].y, E4[r].z, E4[r].w};
-      const float av[4] = {A4[r].x, A4[r].y, A4[r].z, A4[r].w};
-      float nv[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int p = pv[j];
-        const bool valid = ring ? p >= 0 : 4 * q + j < n8;
-        nv[j] = ev[j];
-        int cp = INT_MAX;
-        if (valid) {
-          const float a = fmaf(lam, ev[j], (1.0f - lam) * (av[j] * inv_hq));
-          nv[j] = a;
-          nring += ring;
-          if (p < thr) {
-            cp = p;
-            ++ncand;
-            amin = fminf(amin, a); amax = fmaxf(amax, a);
-            pmin = min(pmin, p); pmax = max(pmax, p);
+        for (int r = 0; r < 2; ++r) {
+          const int q = q0 + r * NT;
+          if (q < nq) {
+            const int slot0 = q < q8 ? 4 * q : cap + 4 * (q - q8);
+            const float4 m = __ldg(reinterpret_cast<const float4*>(mass + (size_t)h * S + slot0));
+            A4[r].x += m.x; A4[r].y += m.y; A4[r].z += m.z; A4[r].w += m.w;
           }
         }
-        if (kSmemKeys) {
-          KEY[slot0 + j] = __float_as_uint(nv[j]);
-          SPOS[slot0 + j] = cp;
+      }
+#pragma unroll
+      for (int r = 0; r < 2; ++r)
+        if (q0 + r * NT < nq) ema_quad(q0 + r * NT, P4[r], E4[r], A4[r]);
+    }
+  } else {
+    // one quad per thread and pass, the KV heads' mass loads issued eight at
+    // a time before they are summed (a short cache: the pass is one round of
+    // loads, so what counts is how many are in flight)
+    for (int q = threadIdx.x; q < nq; q += NT) {
+      const int slot0 = q < q8 ? 4 * q : cap + 4 * (q - q8);
+      const int4 P4 = *reinterpret_cast<const int4*>(pos + slot0);
+      const float4 E4 = *reinterpret_cast<const float4*>(ema + slot0);
+      float4 A4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int h0 = 0; h0 < Hkv; h0 += 8) {
+        float4 m[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          m[j] = h0 + j < Hkv ? __ldcg(reinterpret_cast<const float4*>(mass + (size_t)(h0 + j) * S + slot0))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          A4.x += m[j].x; A4.y += m[j].y; A4.z += m[j].z; A4.w += m[j].w;
         }
       }
-      *reinterpret_cast<float4*>(ema + slot0) = make_float4(nv[0], nv[1], nv[2], nv[3]);
+      ema_quad(q, P4, E4, A4);
     }
   }
   // one combined block reduction of (nring, ncand, amin, amax, pmin, pmax)
@@ -599,7 +628,7 @@ __device__ __forceinline__ void select_group(const Shape s, const Dev d, long lo
   const size_t ustride16 = (size_t)WR * D * 2;          // FP16 ring bytes per unit
   bool req;
   if (k <= 1) {
-    req = tl >= 0 && prs == tl && s_evslot != rslot;
+    req = tl >= 0 && s_prs == tl && s_evslot != rslot;
   } else {
     req = tl >= 0 && pos[rslot] == tl;   // a ring eviction of this step already cleared it
   }
@@ -694,6 +723,14 @@ __device__ __forceinline__ void select_group(const Shape s, const Dev d, long lo
   if (move1) moves = 1;
   const char* k16b = reinterpret_cast<const char*>(d.k16);
   const char* v16b = reinterpret_cast<const char*>(d.v16);
+  // metadata of the move and the requantisation, read by thread 0 before
+  // any of it is written (slot n8 - 1 can be both a source and a target)
+  int mpos = 0;
+  float mema = 0.f, rema = 0.f;
+  if (threadIdx.x == 0) {
+    if (move1) { mpos = pos[src1]; mema = ema[src1]; }
+    if (do_req) rema = ema[rslot];
+  }
   if (move1 || do_req) {
     const size_t sblk = (size_t)(src1 >> 4) * 16 * D, dblk = (size_t)(dst1 >> 4) * 16 * D;
     const size_t qblk = (size_t)(n8p >> 4) * 16 * D;
@@ -702,25 +739,26 @@ __device__ __forceinline__ void select_group(const Shape s, const Dev d, long lo
       const size_t u = u0 + h;
       uint8_t* k8u = d.k8 + u * ustride8;
       uint8_t* v8u = d.v8 + u * ustride8;
+      // every load of this KV head (the move's source, the ring entry and
+      // the scales) before any store: one round of loads instead of two.  A
+      // lane stores only bytes it loaded itself, so the requantisation may
+      // rewrite the move's source slot n8 - 1 without a barrier.
+      uint32_t kv = 0u;
+      uint8_t vb[kVPerLane];
+      uint2 xk = make_uint2(0u, 0u);
+      float2 s01 = make_float2(1.f, 1.f), s89 = make_float2(1.f, 1.f);
+      unsigned short xv[kVPerLane];
+      float sv[kVPerLane];
       if (move1) {
-        uint32_t kv = 0u;
-        uint8_t vb[kVPerLane];
         if (lane < D / 4) kv = *reinterpret_cast<const uint32_t*>(k8u + sblk + k8_offset(D, src1 & 15, kc0));
 #pragma unroll
         for (int i = 0; i < kVPerLane; ++i) vb[i] = v8u[sblk + v8_offset(D, src1 & 15, lane + 32 * i)];
-        if (lane < D / 4) *reinterpret_cast<uint32_t*>(k8u + dblk + k8_offset(D, dst1 & 15, kc0)) = kv;
-#pragma unroll
-        for (int i = 0; i < kVPerLane; ++i) v8u[dblk + v8_offset(D, dst1 & 15, lane + 32 * i)] = vb[i];
       }
       if (do_req) {
         const char* rk = k16b + u * ustride16 + rblk;
         const char* rv = v16b + u * ustride16 + rblk;
         const float* sKu = d.sK + u * D;
         const float* sVu = d.sV + u * D;
-        uint2 xk = make_uint2(0u, 0u);
-        float2 s01 = make_float2(1.f, 1.f), s89 = make_float2(1.f, 1.f);
-        unsigned short xv[kVPerLane];
-        float sv[kVPerLane];
         if (lane < D / 4) {
           xk = *reinterpret_cast<const uint2*>(rk + k16_offset(D, rs & 15, kc0));
           s01 = *reinterpret_cast<const float2*>(sKu + kc0);
@@ -731,6 +769,13 @@ __device__ __forceinline__ void select_group(const Shape s, const Dev d, long lo
           xv[i] = *reinterpret_cast<const unsigned short*>(rv + v16_offset(D, rs & 15, lane + 32 * i));
           sv[i] = sVu[lane + 32 * i];
         }
+      }
+      if (move1) {
+        if (lane < D / 4) *reinterpret_cast<uint32_t*>(k8u + dblk + k8_offset(D, dst1 & 15, kc0)) = kv;
+#pragma unroll
+        for (int i = 0; i < kVPerLane; ++i) v8u[dblk + v8_offset(D, dst1 & 15, lane + 32 * i)] = vb[i];
+      }
+      if (do_req) {
         if (lane < D / 4) {
           const uint32_t w =
               quant_code_sel(__half2float(__ushort_as_half((unsigned short)(xk.x & 0xffffu))), s01.x) |
@@ -747,10 +792,6 @@ __device__ __forceinline__ void select_group(const Shape s, const Dev d, long lo
     }
   }
   if (threadIdx.x == 0) {
-    // metadata: every read before any write (slot n8 - 1 can be both)
-    const int mpos = move1 ? pos[src1] : 0;
-    const float mema = move1 ? ema[src1] : 0.f;
-    const float rema = do_req ? ema[rslot] : 0.f;
     if (k == 1 && dst1 >= cap) pos[dst1] = -1;   // evicted ring entry: the slot becomes empty
     if (move1) { pos[dst1] = mpos; ema[dst1] = mema; }
     if (do_req) { pos[n8p] = tl; ema[n8p] = rema; pos[rslot] = -1; }

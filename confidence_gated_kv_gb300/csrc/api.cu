@@ -76,17 +76,35 @@ Shape make_shape(const confkv_config* c) {
   s.cstride = s.cap + 16;
   // vocabulary chunks per sequence: at most 4096 logits each (16 per thread
   // of a 256-thread prestep block).  Shapes whose every (layer, sequence,
-  // KV head) unit can have an SM of its own (the fused step) take the
-  // smallest chunks from 512 logits up that leave at most one chunk per
-  // unit: one warp of a unit's CTA reduces a chunk while the unit streams.
+  // KV head) unit can have an SM of its own (the fused step):
+  //   - with SMs left over, enough of them to reduce the vocabulary with
+  //     about one warp per 1024 logits or fewer, those SMs take vocabulary
+  //     CTAs, and the chunks are cut to one per warp of those CTAs (at
+  //     least 256 logits each);
+  //   - otherwise the smallest chunks from 512 logits up that leave at most
+  //     one chunk per unit: the epilogue warp of a unit's CTA reduces one
+  //     while the unit streams.
   // Wider vocabularies than kMaxSV chunks are rejected.
   const long long units = (long long)c->L * c->B * c->Hkv;
-  int chunk = 4096;
-  if (units <= attention_persistent_ctas() / 2) {
-    chunk = 512;
-    while (chunk < 4096 && (long long)c->B * ((c->V + chunk - 1) / chunk) > units) chunk *= 2;
+  const long long sms = attention_persistent_ctas() / 2;
+  const long long min_sv = (c->V + 4095) / 4096;
+  long long sv = min_sv;
+  s.vocab_ctas = 0;
+  if (units <= sms) {
+    const long long spare = sms - units;
+    if (spare > 0 && spare * kFusedWarps >= (long long)c->B * ((c->V + 1023) / 1024)) {
+      s.vocab_ctas = (int)spare;
+      sv = std::max(min_sv, std::min(spare * kFusedWarps / c->B, ((long long)c->V + 255) / 256));
+    } else {
+      int chunk = 512;
+      while (chunk < 4096 && (long long)c->B * ((c->V + chunk - 1) / chunk) > units) chunk *= 2;
+      sv = (c->V + chunk - 1) / chunk;
+    }
   }
-  s.SV = std::min(std::max((c->V + chunk - 1) / chunk, 1), kMaxSV);
+  sv = std::min<long long>(std::max<long long>(sv, 1), kMaxSV);
+  // chunks of ceil(V / SV) logits: the count that leaves no chunk empty
+  const long long chunk = (c->V + sv - 1) / sv;
+  s.SV = (int)((c->V + chunk - 1) / chunk);
   s.qbf16 = c->q_dtype == CONFKV_Q_BF16;
   s.max_evict = c->max_evict > 0 ? c->max_evict : s.cap + s.WR;
   s.tau = c->tau; s.wH = c->w_H; s.wm = c->w_m; s.wp = c->w_p;

@@ -676,6 +676,10 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(Shape s, Dev d,
 constexpr int kPConsumers = 4;
 constexpr int kPThreads = (kPConsumers + 2) * 32;
 constexpr int kPMaxStages = 12;
+// mbarriers of the persistent kernel: full and empty per stage, header full
+// and empty, done and efree (two each), and the fused step's append; an even
+// count keeps the shared ints after them 16-byte aligned
+constexpr int kPBars = 2 * kPMaxStages + 10;
 
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
@@ -792,19 +796,33 @@ __device__ __forceinline__ int next_unit(const Shape& s, const Dev& d, int units
   return u < units ? u : -1;
 }
 
+// Fused step: the stage that the producer issues, and the consumers take,
+// i-th.  The INT8 stages come first, then the ring stages with the one that
+// holds this step's new token (ring stage jnew) moved last: every other
+// stage can be issued before the new token is appended, and only the last
+// one has to follow the append.
+__device__ __forceinline__ int fused_stage(int i, int n8st, int nst, int jnew) {
+  if (i < n8st) return i;
+  const int k = i - n8st;
+  if (k == nst - 1 - n8st) return n8st + jnew;
+  return n8st + (k < jnew ? k : k + 1);
+}
+
 // Modes of the persistent kernel.
 //   kModeAttention    attention and mass only (prestep and select run as
 //                     kernels of their own);
 //   kModeFused        the whole decode step in one launch for shapes whose
-//                     units and vocabulary chunks fit one wave: CTAs
-//                     [0, units) take one unit each and append its new token
-//                     first; CTAs [units, units + B * SV) reduce one
-//                     vocabulary chunk each, and the last chunk of a sequence
-//                     merges its confidence and budgets.  Each (layer,
-//                     sequence) counts Hkv unit arrivals and one confidence
-//                     arrival; the CTA that makes the last one runs that
-//                     group's selection (select_body.cuh) once its own work is
-//                     done.  No CTA waits for another.
+//                     units fit one CTA per SM: CTAs [0, units) take one
+//                     unit each and append its new token; the vocabulary
+//                     chunks go to the warps of the CTAs after them (SMs the
+//                     units leave free, Shape::vocab_ctas), or, with no SM to
+//                     spare, one chunk to the epilogue warp of each of the
+//                     first B * SV unit CTAs.  The warp that completes a
+//                     sequence's chunks merges its confidence and budgets.
+//                     Each (layer, sequence) counts Hkv unit arrivals and one
+//                     confidence arrival; the CTA that makes the last one
+//                     runs that group's selection (select_body.cuh) once its
+//                     own work is done.  No CTA waits for another.
 //   kModeFusedDevStep the same, with the step index read from the device (a
 //                     step inside a graph reservation).
 enum : int { kModeAttention = 0, kModeFused = 1, kModeFusedDevStep = 2 };
@@ -824,7 +842,13 @@ struct FusedArgs {
 // layout from kFusedSelOff.
 constexpr int kFusedSelOff = 2048;
 // Shared ints before the fused step's selection list (s_misc[kFusedMiscInts]).
-constexpr int kFusedMiscInts = 24;
+constexpr int kFusedMiscInts = 8;
+// Bytes of the persistent kernel's shared ints (abort flag, unit indices,
+// the fused step's selection list of up to L * B + 2 groups), a multiple of
+// 16: a fused step's score slot follows them.
+__host__ __device__ inline int misc_bytes(const Shape& s) {
+  return ((kFusedMiscInts + s.L * s.B + 2) * 4 + 15) / 16 * 16;
+}
 static_assert(sizeof(SelShared) <= kFusedSelOff, "SelShared fits below the selection area");
 
 template <int D, bool kFlush, int kMode, int NC>
@@ -846,7 +870,7 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
   float* wpart = reinterpret_cast<float*>(hbuf + 2 * hl.bytes);            // [2][4][G][D + 2]
   const int part_floats = NC * G * (D + 2);
   uint64_t* bars = reinterpret_cast<uint64_t*>(wpart + 2 * part_floats);
-  int* s_misc = reinterpret_cast<int*>(bars + 2 * kPMaxStages + 10);
+  int* s_misc = reinterpret_cast<int*>(bars + kPBars);
   int& s_abort = s_misc[0];
   // unit index of header slot hs (set by the producer before its arrival on
   // hfull) and of partials slot ps (set by consumer warp 0 before its arrival
@@ -854,13 +878,13 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
   volatile int* s_unit = s_misc + 1;    // [2]
   volatile int* s_eunit = s_misc + 3;   // [2]
   // fused step: the (layer, sequence) groups whose selection falls to this
-  // CTA: s_nsel of them in s_sel (at most L + 1: every layer of a sequence
-  // whose confidence this CTA merged, and the group of its own unit)
+  // CTA: s_nsel of them in s_sel (room for L * B + 2; each group has one
+  // last arrival, so no CTA lists more than L * B)
   volatile int* s_nsel = s_misc + 5;
   volatile int* s_sel = s_misc + kFusedMiscInts;
-  // fused step: the unit's Mg[8], 1 / Lg[8] for the consumer warps' share of
-  // the mass loop
-  float* s_mass = reinterpret_cast<float*>(s_misc + 8);
+  // fused step: the ring stage holding the new token's slot (fused_stage),
+  // set by the producer before its arrival on header slot 0
+  volatile int* s_jnew = s_misc + 6;
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
   auto empty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(kPMaxStages + i); };
@@ -868,12 +892,14 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
   auto hempty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * kPMaxStages + 2 + i); };
   auto done_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * kPMaxStages + 4 + i); };
   auto efree_bar = [&](int i) { return bar0 + 8u * (uint32_t)(2 * kPMaxStages + 6 + i); };
-  // fused step: s_mass published (1 arrival), the mass loop shared by the
-  // consumer warps and the epilogue warp done (5 arrivals)
-  const uint32_t mready_bar = bar0 + 8u * (uint32_t)(2 * kPMaxStages + 8);
-  const uint32_t mdone_bar = bar0 + 8u * (uint32_t)(2 * kPMaxStages + 9);
-  // this CTA's two score slots: [2][G][S] (token index = slot index in the unit)
-  float* scg_base = d.scores + (size_t)blockIdx.x * 2 * G * s.S;
+  // fused step: the new token appended (by the epilogue warp) and made
+  // visible to bulk copies
+  const uint32_t app_bar = bar0 + 8u * (uint32_t)(2 * kPMaxStages + 8);
+  // this CTA's two score slots: [2][G][S] (token index = slot index in the
+  // unit); a fused step keeps its one unit's scores in shared memory, after
+  // the shared ints
+  float* scg_base = kFused ? reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(s_misc) + misc_bytes(s))
+                           : d.scores + (size_t)blockIdx.x * 2 * G * s.S;
 
   const int units = s.L * s.B * s.Hkv;
   const int nbR = s.WR >> 4;
@@ -896,8 +922,7 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
       mbar_init(done_bar(i), NC);
       mbar_init(efree_bar(i), 1);
     }
-    mbar_init(mready_bar, 1);
-    mbar_init(mdone_bar, NC + 1);
+    mbar_init(app_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
@@ -913,7 +938,10 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
   // selection.  (Called by several threads of the CTA: the list grows with
   // a shared atomic.)
   auto arrive_group = [&](int lb) {
-    if (atomicAdd(d.arrive + lb, 1u) == (unsigned)s.Hkv) s_sel[atomicAdd((int*)s_nsel, 1)] = lb;
+    if (atomicAdd(d.arrive + lb, 1u) == (unsigned)s.Hkv) {
+      __threadfence();   // acquire: the other arrivals' writes are visible to this CTA's selection
+      s_sel[atomicAdd((int*)s_nsel, 1)] = lb;
+    }
   };
 
   // End of this CTA's work: in a fused step, every warp meets here once its
@@ -954,8 +982,12 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
       const int slot = v < nb8 * 16 ? v : s.cap + (v - nb8 * 16);
       float4 sv[kMaxG];
 #pragma unroll
-      for (int gg = 0; gg < kMaxG; ++gg)
-        if (gg < G) sv[gg] = __ldcs(reinterpret_cast<const float4*>(scg + (size_t)gg * s.S + slot));
+      for (int gg = 0; gg < kMaxG; ++gg) {
+        if (gg < G) {
+          const float4* src = reinterpret_cast<const float4*>(scg + (size_t)gg * s.S + slot);
+          sv[gg] = kFused ? *src : __ldcs(src);
+        }
+      }
       float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int gg = 0; gg < kMaxG; ++gg) {
@@ -970,21 +1002,78 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
     }
   };
 
+  // Fused step: vocabulary chunk c (sequence c / SV) by this warp.  The
+  // warp that completes a sequence's chunks merges its confidence and
+  // budgets and counts one arrival on every layer of the sequence (one lane
+  // per layer).
+  auto vocab_chunk = [&](int c) {
+    const int bc = c / s.SV;
+    conf_partial_warp(s, d, logits, bc, c % s.SV);
+    unsigned int prev = 0;
+    if (lane == 0) {
+      __threadfence();
+      prev = atomicAdd(d.conf_done + bc, 1u);
+    }
+    prev = __shfl_sync(0xffffffffu, prev, 0);
+    if (prev == (unsigned int)s.SV - 1u) {
+      __threadfence();
+      conf_merge_warp(s, d, bc, budget, conf_out);
+      if (lane == 0) d.conf_done[bc] = 0u;   // zero again for the next launch
+      __syncwarp();
+      __threadfence();   // the budgets and c are visible before any arrival
+      for (int ll = lane; ll < s.L; ll += 32) arrive_group(ll * s.B + bc);
+    }
+  };
+
+  if constexpr (kFused) {
+    if ((int)blockIdx.x < units && warp == NC + 1) {
+      // The epilogue warp, idle until the unit is streamed, appends the new
+      // token to the unit's ring slot; the proxy fence orders those stores
+      // before the bulk copy (async proxy) of the ring stage that reads them
+      // back, which the producer issues last, after this arrival.
+      const int u = blockIdx.x;
+      const int b = (u / s.Hkv) % s.B;
+      append_unit_warp<D>(s, d, u, d.T0[b] + (int)fstep, fa.k_new, fa.v_new);
+      asm volatile("fence.proxy.async.global;\n" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(app_bar);
+    }
+    // Vocabulary chunks.  CTAs after the units (on SMs the units leave free)
+    // reduce them with all their warps, so the confidence is merged while
+    // the units stream and no unit's epilogue warp waits for it.  With no
+    // such CTA, the epilogue warp of unit CTA c < B * SV reduces chunk c
+    // while the consumer warps stream the unit; chunks are small (512
+    // logits), so this comes before the units finish, and the last arrival
+    // of a group, with its selection, falls to the CTA of one of its units.
+    const bool vocab_cta = (int)blockIdx.x >= units;
+    if (vocab_cta || (warp == NC + 1 && s.vocab_ctas == 0)) {
+      const int nw = NTH / 32;
+      const int c0 = vocab_cta ? ((int)blockIdx.x - units) * nw + warp : (int)blockIdx.x;
+      const int stride = vocab_cta ? s.vocab_ctas * nw : s.B * s.SV;
+      for (int c = c0; c < s.B * s.SV; c += stride) vocab_chunk(c);
+    }
+    if (vocab_cta) {
+      finish();
+      return;
+    }
+  }
+
   if (warp == NC) {
     // ------------------------------------------------ producer warp
     if constexpr (kFused) {
       // Fused step: this CTA's one unit, u = blockIdx.x.  The header (q and
-      // the scales) and the INT8 blocks do not depend on this step's new
-      // token, so their bulk copies go first; then the whole warp appends
-      // the new token to its ring slot, and the proxy fence orders those
-      // stores before the ring blocks' bulk copies (async proxy) read them
-      // back.  The consumers read the ring positions from global memory
-      // (after the ring stage's barrier), not from the header.
+      // the scales) and every stage but the ring stage holding the new
+      // token's slot do not depend on this step's new token; that stage
+      // comes last (fused_stage), once the epilogue warp has appended the
+      // token (app_bar).  The consumers read the ring positions from global
+      // memory (after the ring stage's barrier), not from the header.
       const uint64_t pol = policy_evict_first();
       const int u = blockIdx.x;
       const int h = u % s.Hkv, b = (u / s.Hkv) % s.B, l = u / (s.Hkv * s.B);
       const size_t lb = lb_index(s, l, b);
       const int nb8 = (d.n8[lb] + 15) >> 4;
+      const int t_new = d.T0[b] + (int)fstep;
+      const int jnew = ((t_new % s.WR) >> 4) >> 1;
       Sched sch;
       sch.init(0, nb8 + nbR, nb8);
       const char* k8u = reinterpret_cast<const char*>(d.k8) + (size_t)u * s.cstride * D;
@@ -998,7 +1087,7 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
         if (issued >= stages && !mbar_wait(empty_bar(st.slot), st.phase ^ 1u)) return false;
         bool ring;
         int first, nb;
-        sch.first_last(i, ring, first, nb);
+        sch.first_last(fused_stage(i, sch.n8st, sch.nst, jnew), ring, first, nb);
         const uint32_t span = (uint32_t)(nb * 16 * D * (ring ? 2 : 1));
         const char* ksrc = ring ? k16u + (size_t)first * 32 * D : k8u + (size_t)first * 16 * D;
         const char* vsrc = ring ? v16u + (size_t)first * 32 * D : v8u + (size_t)first * 16 * D;
@@ -1012,6 +1101,7 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
       };
       if (lane == 0) {
         s_unit[0] = u;
+        s_jnew[0] = jnew;
         const uint32_t hdst = smem_u32(hbuf);
         const uint32_t qbytes = (uint32_t)(G * D * 2);
         mbar_arrive_tx(hfull_bar(0), qbytes + 2u * D * 4);
@@ -1019,17 +1109,11 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
                  hfull_bar(0));
         bulk_g2s(hdst + hl.sk, d.sK + (size_t)u * D, D * 4, hfull_bar(0));
         bulk_g2s(hdst + hl.sv, d.sV + (size_t)u * D, D * 4, hfull_bar(0));
-        for (int i = 0; i < sch.n8st && ok; ++i) ok = issue(i);
-      }
-      append_unit_warp<D>(s, d, u, d.T0[b] + (int)fstep, fa.k_new, fa.v_new);
-      asm volatile("fence.proxy.async.global;\n" ::: "memory");
-      __syncwarp();
-      if (lane == 0) {
-        for (int i = sch.n8st; i < sch.nst && ok; ++i) ok = issue(i);
+        for (int i = 0; i < sch.nst && ok; ++i) {
+          if (i == sch.nst - 1 && !mbar_wait(app_bar, 0)) ok = false;
+          if (ok) ok = issue(i);
+        }
         if (!ok) fail();
-        // no second unit: the other warps see -1 in header slot 1
-        s_unit[1] = -1;
-        mbar_arrive(hfull_bar(1));
       }
       if (lane == 0) {
         // wait (bounded) for the last copy of every stage slot
@@ -1115,37 +1199,14 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
 
   if (warp == NC + 1) {
     // ------------------------------------------------ epilogue warp
+    if constexpr (kFused) {
+      // fused step: the append and the vocabulary chunk, if any, are done
+      // (above); the consumer warps finish the unit themselves
+      finish();
+      return;
+    }
     // Idle until the first unit is done: the confidence of the step.
-    if (kFused) {
-      // Fused step: this warp reduces CTA c's vocabulary chunk (c < B * SV,
-      // at most one per CTA) while the consumer warps stream the unit.  The
-      // CTA that completes a sequence's chunks merges its confidence and
-      // budgets and counts one arrival on every layer of the sequence (one
-      // lane per layer).  Chunks are small (512 logits), so this comes before
-      // the units finish, and the last arrival of a group, with its
-      // selection, falls to the CTA of one of its units.
-      const int c = blockIdx.x;
-      if (c < s.B * s.SV) {
-        const int bc = c / s.SV;
-        conf_partial_warp(s, d, logits, bc, c % s.SV);
-        unsigned int prev = 0;
-        if (lane == 0) {
-          __threadfence();
-          prev = atomicAdd(d.conf_done + bc, 1u);
-        }
-        prev = __shfl_sync(0xffffffffu, prev, 0);
-        if (prev == (unsigned int)s.SV - 1u) {
-          __threadfence();
-          conf_merge_warp(s, d, bc, budget, conf_out);
-          if (lane == 0) {
-            d.conf_done[bc] = 0u;   // zero again for the next launch
-            __threadfence();
-          }
-          __syncwarp();
-          for (int ll = lane; ll < s.L; ll += 32) arrive_group(ll * s.B + bc);
-        }
-      }
-    } else if (logits) {
+    if (logits) {
       // Logits in host memory: this CTA reduces its vocabulary chunks to
       // partials here, so that their transfer overlaps the attention; the
       // CTA that finishes the last chunk of a sequence merges that sequence.
@@ -1215,29 +1276,7 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
       float invL[kMaxG];
 #pragma unroll
       for (int gg = 0; gg < kMaxG; ++gg) invL[gg] = gg < G ? 1.0f / Lg[gg] : 0.f;
-      if constexpr (kFused) {
-        // this CTA's only unit: the four consumer warps, idle now, take four
-        // fifths of the mass loop; the arrival on the unit's (layer,
-        // sequence) follows every share
-        if (lane == 0) {
-#pragma unroll
-          for (int gg = 0; gg < kMaxG; ++gg) {
-            s_mass[gg] = Mg[gg];
-            s_mass[kMaxG + gg] = invL[gg];
-          }
-          mbar_arrive(mready_bar);
-        }
-        mass_quads(u, nb8, scg, Mg, invL, NC * 32 + lane, (NC + 1) * 32);
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(mdone_bar);
-        // every share's stores were made visible by its own warp's fence
-        // before that warp arrived
-        if (!mbar_wait(mdone_bar, 0)) fail();
-        if (lane == 0 && !aborted()) arrive_group((int)lb);
-      } else {
-        mass_quads(u, nb8, scg, Mg, invL, lane, 32);
-      }
+      mass_quads(u, nb8, scg, Mg, invL, lane, 32);
       __syncwarp();
       if (lane == 0) mbar_arrive(efree_bar(ps));
     }
@@ -1249,6 +1288,7 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
   const float qs = kQPre * 1.4426950408889634f * rsqrtf((float)D);
   const uint64_t keep = policy_evict_last();
   RingPos st;
+  int fused_nb8 = 0;   // fused step: INT8 blocks of the CTA's unit
   for (int k = 0;; ++k) {
     const int hs = k & 1;
     if (aborted() || !mbar_wait(hfull_bar(hs), (uint32_t)((k >> 1) & 1))) {
@@ -1271,6 +1311,7 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
     const size_t lb = lb_index(s, l, b);
     const int n8 = d.n8[lb];
     const int nb8 = (n8 + 15) >> 4;
+    fused_nb8 = nb8;
     const unsigned char* hdr = hbuf + (size_t)hs * hl.bytes;
     const float* sKh = reinterpret_cast<const float*>(hdr + hl.sk);
     const float* sVh = reinterpret_cast<const float*>(hdr + hl.sv);
@@ -1294,7 +1335,9 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
       if (!mbar_wait(full_bar(st.slot), st.phase)) { ok = false; break; }
       bool ring;
       int first, nb;
-      sch.first_last(i, ring, first, nb);
+      // fused step: the producer's stage order (the new token's ring stage last)
+      sch.first_last((kFused && i >= sch.n8st) ? fused_stage(i, sch.n8st, sch.nst, s_jnew[0]) : i, ring, first,
+                     nb);
       const uint32_t stage = smem_u32(sbuf + (size_t)st.slot * kStageBytes);
       int tok0 = -1;
       if (!ring) {
@@ -1330,10 +1373,16 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
       if (tok0 >= 0 && g < G) {
         // raw scores of tokens tok0 + {2t, 2t+1, 8+2t, 9+2t} of head g
         float* dst = scg + (size_t)g * s.S + tok0 + 2 * t;
-        asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;\n" ::"l"(dst),
-                     "f"(sc4buf[0]), "f"(sc4buf[1]), "l"(keep) : "memory");
-        asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;\n" ::"l"(dst + 8),
-                     "f"(sc4buf[2]), "f"(sc4buf[3]), "l"(keep) : "memory");
+        if constexpr (kFused) {
+          // the unit's score slot in shared memory
+          *reinterpret_cast<float2*>(dst) = make_float2(sc4buf[0], sc4buf[1]);
+          *reinterpret_cast<float2*>(dst + 8) = make_float2(sc4buf[2], sc4buf[3]);
+        } else {
+          asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;\n" ::"l"(dst),
+                       "f"(sc4buf[0]), "f"(sc4buf[1]), "l"(keep) : "memory");
+          asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;\n" ::"l"(dst + 8),
+                       "f"(sc4buf[2]), "f"(sc4buf[3]), "l"(keep) : "memory");
+        }
       }
     }
     if (!ok) {
@@ -1357,6 +1406,8 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
         pw[D + 1] = lsum;
       }
     }
+    // fused step: one unit only; the consumer warps finish it below
+    if constexpr (kFused) break;
     __syncwarp();
     if (lane == 0) {
       mbar_arrive(done_bar(hs));
@@ -1364,26 +1415,62 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
     }
   }
   if constexpr (kFused) {
-    // the consumer warps' share of the mass loop of this CTA's only unit
-    // (unit index in header slot 0), once the epilogue warp has published
-    // the unit's maxima and normalisers
-    const int u0 = s_unit[0];
-    if (u0 >= 0 && !aborted()) {
-      if (mbar_wait(mready_bar, 0)) {
-        float Mg[kMaxG], invL[kMaxG];
+    // Fused step: the consumer warps finish this CTA's only unit, u =
+    // blockIdx.x: merge their partials, write the output and the tokens'
+    // attention mass (scores in shared memory), and count the unit's arrival
+    // on its (layer, sequence).  Every consumer warp reaches both named
+    // barriers, whether or not a bounded wait above gave up.
+    named_sync(1, NC * 32);
+    const int u = blockIdx.x;
+    const int h = u % s.Hkv, b = (u / s.Hkv) % s.B, l = u / (s.Hkv * s.B);
+    const size_t lb = lb_index(s, l, b);
+    if (!aborted()) {
+      const int tid = threadIdx.x;
+      const float* part = wpart;   // slot 0: [NC][G][D + 2] = o..., m, l
+      float Mg[kMaxG], invL[kMaxG];
+#pragma unroll
+      for (int gg = 0; gg < kMaxG; ++gg) {
+        Mg[gg] = 0.f;
+        invL[gg] = 0.f;
+        if (gg < G) {
+          float m = -INFINITY;
+#pragma unroll
+          for (int w = 0; w < NC; ++w) m = fmaxf(m, part[(w * G + gg) * (D + 2) + D]);
+          float lsum = 0.f;
+#pragma unroll
+          for (int w = 0; w < NC; ++w) {
+            const float mw = part[(w * G + gg) * (D + 2) + D];
+            lsum += mw == -INFINITY ? 0.f : part[(w * G + gg) * (D + 2) + D + 1] * ex2(mw - m);
+          }
+          Mg[gg] = m;
+          invL[gg] = 1.0f / lsum;
+        }
+      }
+      // output: channel tid of every head (D <= NC * 32)
+      if (tid < D) {
+        float* o = out + (lb * s.Hq + (size_t)h * G) * D;
 #pragma unroll
         for (int gg = 0; gg < kMaxG; ++gg) {
-          Mg[gg] = s_mass[gg];
-          invL[gg] = s_mass[kMaxG + gg];
+          if (gg < G) {
+            float acc = 0.f;
+#pragma unroll
+            for (int w = 0; w < NC; ++w) {
+              const float mw = part[(w * G + gg) * (D + 2) + D];
+              if (mw != -INFINITY) acc += part[(w * G + gg) * (D + 2) + tid] * ex2(mw - Mg[gg]);
+            }
+            o[gg * D + tid] = acc * invL[gg];
+          }
         }
-        const int nb8 = (d.n8[u0 / s.Hkv] + 15) >> 4;
-        mass_quads(u0, nb8, scg_base, Mg, invL, (int)threadIdx.x, (NC + 1) * 32);
-        __threadfence();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(mdone_bar);
-      } else {
-        fail();
       }
+      mass_quads(u, fused_nb8, scg_base, Mg, invL, tid, NC * 32);
+    }
+    named_sync(1, NC * 32);
+    // every consumer thread's mass stores come before the barrier; this
+    // fence (cumulative) makes them visible at GPU scope before the group
+    // arrival that may start the group's selection in another CTA
+    if (threadIdx.x == 0 && !aborted()) {
+      __threadfence();
+      arrive_group((int)lb);
     }
   }
   finish();
@@ -1407,16 +1494,18 @@ static int fixed_bytes_split(const Shape& s, int splits, int max_tokens) {
   return (int)(f * sizeof(float)) + 2 * kMaxStages * 8;
 }
 
-// Fused steps run the persistent kernel with 8 consumer warps, one CTA per
-// SM (every unit on an SM of its own); the attention-only launch with 4,
-// two CTAs per SM.
-constexpr int kFusedConsumers = 8;
+// Fused steps run the persistent kernel with kFusedConsumers (8) consumer
+// warps, one CTA per SM (every unit on an SM of its own); the
+// attention-only launch with 4, two CTAs per SM.
 
+// Shared memory besides the stages: two headers, two partials slots, the
+// mbarriers, the shared ints and, in a fused step (nc = kFusedConsumers),
+// the unit's score slot G x S.
 static int fixed_bytes_persistent(const Shape& s, int nc = kPConsumers) {
   const HeaderLayout hl(s.G, s.D, s.WR);
   const int part = nc * s.G * (s.D + 2) * 4;
-  const int misc = ((kFusedMiscInts + s.L + 2) * 4 + 15) / 16 * 16;
-  return 2 * hl.bytes + 2 * part + (2 * kPMaxStages + 10) * 8 + misc;
+  const int scores = nc == kFusedConsumers ? (s.G * s.S * 4 + 15) / 16 * 16 : 0;
+  return 2 * hl.bytes + 2 * part + kPBars * 8 + misc_bytes(s) + scores;
 }
 
 int attention_max_smem() { return 225 * 1024; }
@@ -1558,13 +1647,15 @@ static int launch_d(const Shape& s, const Dev& d, const void* q, float* out, int
 bool fused_step_fits(const Shape& s, const Dev& d, int splits, int max_tokens) {
   const long long units = (long long)s.L * s.B * s.Hkv;
   if (splits != 1 || s.compaction != 0) return false;
-  if (units > attention_persistent_ctas() / 2) return false;
-  // each CTA's epilogue warp reduces at most one vocabulary chunk, so it
-  // merges at most one sequence (its selection list holds L + 1 groups)
-  if ((long long)s.B * s.SV > units) return false;
+  if (units + s.vocab_ctas > attention_persistent_ctas() / 2) return false;
+  // without vocabulary CTAs each unit CTA's epilogue warp reduces at most
+  // one vocabulary chunk
+  if (s.vocab_ctas == 0 && (long long)s.B * s.SV > units) return false;
   if (d.attn_ctas > 0 && units > d.attn_ctas) return false;
   if (units > d.score_ctas) return false;
   if (max_tokens - s.WR > kFlushTokens) return false;
+  // two stages at least beside the unit's score slot and the rest
+  if (fixed_bytes_persistent(s, kFusedConsumers) + 2 * stage_bytes(s.D) > attention_max_smem()) return false;
   const SelSmem sm = plan_select(s);
   if (sm.off_key < 0) return false;
   const long long need = kFusedSelOff + ((sm.bytes + 127) & ~127);
@@ -1582,7 +1673,7 @@ static int launch_fused_d(const Shape& s, const Dev& d, long long step, const vo
   if (ensure_smem(kern, attention_max_smem(), configured[dev]) != cudaSuccess) return -1;
   const int stages = stages_persistent(s, kFusedConsumers);
   const int smem = stages * stage_bytes(D) + fixed_bytes_persistent(s, kFusedConsumers);
-  const int grid = s.L * s.B * s.Hkv;
+  const int grid = s.L * s.B * s.Hkv + s.vocab_ctas;
   FusedArgs fa{};
   fa.step = step;
   fa.k_new = static_cast<const __half*>(k_new);

@@ -116,6 +116,8 @@ struct Shape {
   double tau, wH, wm, wp;     // confidence weights and threshold (float64 math)
   float alpha, lam;           // rank weight and EMA decay (float32 math)
   int compaction;             // 0 tail fill, 1 order preserving (ablation)
+  int vocab_ctas;             // fused step: CTAs after the units that only reduce vocabulary
+                              // chunks (0: the units' epilogue warps reduce one chunk each)
 };
 
 struct Dev {
@@ -289,6 +291,9 @@ int launch_fused_step(const Shape& s, const Dev& d, long long step, const void* 
                       int32_t* evicted_pos, int32_t* n_evicted, int max_tokens, cudaStream_t stream);
 int attention_max_smem();
 int attention_persistent_ctas();   // persistent CTAs per launch (2 per SM)
+// Warps of a fused-step CTA: 8 consumer warps, the producer and the epilogue warp.
+constexpr int kFusedConsumers = 8;
+constexpr int kFusedWarps = kFusedConsumers + 2;
 int launch_selftest_timeout(const Dev& d, cudaStream_t stream);
 
 }  // namespace confkv

@@ -269,6 +269,22 @@ def test_gpt2_small_batch1_full_trajectory(mode):
     assert p.flags.max_out_err <= 2e-3
 
 
+@pytest.mark.parametrize("mode", MODES, ids=MODE_IDS)
+def test_fused_step_with_no_sm_to_spare(mode):
+    # As many units as SMs: no CTA is left for the vocabulary, so the units'
+    # epilogue warps reduce the chunks (one each) in the fused step.
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    Hkv = 8 if sms % 8 == 0 else 4 if sms % 4 == 0 else 0
+    if Hkv == 0 or sms // Hkv > 64:
+        pytest.skip("needs an SM count with a small divisor")
+    L = sms // Hkv
+    w = Workload(name="t_nospare", B=1, L=L, Hq=2 * Hkv, Hkv=Hkv, d=64, V=5000, T0=90, steps=12,
+                 n_high=(32,) * L, n_low=(64,) * L, P=8, W=32, q_dtype="f16")
+    p = _run(w, 17, 12, confident_every=4, mode=mode)
+    assert p.cache.step_launches() == (1 if mode == ck.binding.STEP_AUTO else 3)
+    assert p.flags.evictions > 0
+
+
 def test_gpt2_small_batch8_pyramid_prefix():
     w = get_workload("gpt2_b8_pyramid")
     p = _run(w, 1002, 24, confident_every=6, check_state=False)

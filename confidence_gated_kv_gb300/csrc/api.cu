@@ -80,7 +80,8 @@ Shape make_shape(const confkv_config* c) {
   //   - with SMs left over, enough of them to reduce the vocabulary with
   //     about one warp per 1024 logits or fewer, those SMs take vocabulary
   //     CTAs, and the chunks are cut to one per warp of those CTAs (at
-  //     least 256 logits each);
+  //     least 256 logits each): each warp loads its chunk in one round, and
+  //     the confidence is merged long before the units' attention ends;
   //   - otherwise the smallest chunks from 512 logits up that leave at most
   //     one chunk per unit: the epilogue warp of a unit's CTA reduces one
   //     while the unit streams.
@@ -147,6 +148,7 @@ size_t layout(const Shape& s, char* base, Dev* d, Staging* st) {
   dd.order = cv.take<int32_t>(lbs);
   dd.queue = cv.take<uint32_t>(1);
   dd.arrive = cv.take<uint32_t>(lbs);
+  dd.conf_ready = cv.take<uint32_t>(s.B);
   // the persistent attention kernel takes its units longest first from a
   // queue over prestep's sorted order (round robin when there are too many
   // groups to sort in one prestep launch)
@@ -258,6 +260,7 @@ int confkv_create(const confkv_config* cfg, void* workspace, size_t workspace_by
   if (e == cudaSuccess) e = cudaMemset(c->d.sel_done, 0, sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(c->d.conf_done, 0, s.B * sizeof(uint32_t));
   if (e == cudaSuccess) e = cudaMemset(c->d.arrive, 0, (size_t)s.L * s.B * sizeof(uint32_t));
+  if (e == cudaSuccess) e = cudaMemset(c->d.conf_ready, 0, s.B * sizeof(uint32_t));
   if (e != cudaSuccess) {
     delete c;
     return CONFKV_ECUDA;
@@ -300,6 +303,8 @@ int confkv_prefill(confkv_ctx* ctx, const int32_t* prefill_len, const void* k, c
   if (e == cudaSuccess) e = cudaMemsetAsync(ctx->d.sel_done, 0, sizeof(uint32_t), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(ctx->d.conf_done, 0, s.B * sizeof(uint32_t), st);
   if (e == cudaSuccess) e = cudaMemsetAsync(ctx->d.arrive, 0, (size_t)s.L * s.B * sizeof(uint32_t), st);
+  // the step indices start again from 0: no flag of the earlier steps may match
+  if (e == cudaSuccess) e = cudaMemsetAsync(ctx->d.conf_ready, 0, s.B * sizeof(uint32_t), st);
   if (e != cudaSuccess) return CONFKV_ECUDA;
   if (launch_prefill(s, ctx->d, k, v, t_max, ctx->T0.data(), st) != 0) return CONFKV_ECUDA;
   // the host copy of T0 is pageable: make sure it has been consumed

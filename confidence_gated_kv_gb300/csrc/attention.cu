@@ -78,6 +78,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;\n" ::"l"(p), "r"(v) : "memory");
+}
 // Bounded wait: false after kSpinLimit polls.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
   for (long long i = 0; i < kSpinLimit; ++i)
@@ -787,10 +795,13 @@ __device__ __forceinline__ int unit_of_rank(const Shape& s, const Dev& d, int un
 //                     remaining units: the longest-first queue evens out the
 //                     CTAs' end times.
 //   kSchedRoundRobin  u = blockIdx.x + k * gridDim.x (groups not sorted).
-//   fused step        CTA i < units takes unit i, and only that one.
+//   fused step        CTA vocab_ctas + i takes unit i, and only that one.
 template <bool kFused>
 __device__ __forceinline__ int next_unit(const Shape& s, const Dev& d, int units, int k) {
-  if (kFused) return (k == 0 && (int)blockIdx.x < units) ? (int)blockIdx.x : -1;
+  if (kFused) {
+    const int u = (int)blockIdx.x - s.vocab_ctas;
+    return (k == 0 && u >= 0 && u < units) ? u : -1;
+  }
   if (d.sched == kSchedQueue) return unit_of_rank(s, d, units, (int)atomicAdd(d.queue, 1u));
   const int u = (int)blockIdx.x + k * (int)gridDim.x;
   return u < units ? u : -1;
@@ -812,17 +823,19 @@ __device__ __forceinline__ int fused_stage(int i, int n8st, int nst, int jnew) {
 //   kModeAttention    attention and mass only (prestep and select run as
 //                     kernels of their own);
 //   kModeFused        the whole decode step in one launch for shapes whose
-//                     units fit one CTA per SM: CTAs [0, units) take one
-//                     unit each and append its new token; the vocabulary
-//                     chunks go to the warps of the CTAs after them (SMs the
-//                     units leave free, Shape::vocab_ctas), or, with no SM to
-//                     spare, one chunk to the epilogue warp of each of the
-//                     first B * SV unit CTAs.  The warp that completes a
-//                     sequence's chunks merges its confidence and budgets.
-//                     Each (layer, sequence) counts Hkv unit arrivals and one
-//                     confidence arrival; the CTA that makes the last one
-//                     runs that group's selection (select_body.cuh) once its
-//                     own work is done.  No CTA waits for another.
+//                     units fit one CTA per SM: the first vocab_ctas CTAs
+//                     (SMs the units leave free) reduce the vocabulary
+//                     chunks with all their warps; with no SM to spare, the
+//                     epilogue warps of the first B * SV unit CTAs take one
+//                     chunk each.  The warp that completes a sequence's
+//                     chunks merges its confidence and budgets and flags
+//                     them (release).  Each unit CTA appends its new token,
+//                     streams its unit and counts one arrival on its (layer,
+//                     sequence); the CTA that makes a group's last arrival
+//                     runs its selection (select_body.cuh) once its own work
+//                     is done, after a bounded wait for the sequence's flag.
+//                     The CTAs that reduce the vocabulary come first and wait
+//                     on nothing, so that wait always ends.
 //   kModeFusedDevStep the same, with the step index read from the device (a
 //                     step inside a graph reservation).
 enum : int { kModeAttention = 0, kModeFused = 1, kModeFusedDevStep = 2 };
@@ -841,8 +854,9 @@ struct FusedArgs {
 // work, reusing the stage area): SelShared at 0, the selection's dynamic
 // layout from kFusedSelOff.
 constexpr int kFusedSelOff = 2048;
+
 // Shared ints before the fused step's selection list (s_misc[kFusedMiscInts]).
-constexpr int kFusedMiscInts = 8;
+constexpr int kFusedMiscInts = 24;
 // Bytes of the persistent kernel's shared ints (abort flag, unit indices,
 // the fused step's selection list of up to L * B + 2 groups), a multiple of
 // 16: a fused step's score slot follows them.
@@ -885,6 +899,8 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
   // fused step: the ring stage holding the new token's slot (fused_stage),
   // set by the producer before its arrival on header slot 0
   volatile int* s_jnew = s_misc + 6;
+  // fused step: the unit's maxima Mg[kMaxG] and 1 / Lg[kMaxG]
+  float* s_stat = reinterpret_cast<float*>(s_misc + 8);
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
   auto empty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(kPMaxStages + i); };
@@ -933,12 +949,10 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
   };
   auto aborted = [&](void) { return *(volatile int*)&s_abort != 0; };
 
-  // One arrival on (layer, sequence) lb; the CTA that makes the last one
-  // (Hkv unit arrivals and one confidence arrival) runs the group's
-  // selection.  (Called by several threads of the CTA: the list grows with
-  // a shared atomic.)
+  // One unit's arrival on (layer, sequence) lb; the CTA that makes the last
+  // of the Hkv runs the group's selection (finish).
   auto arrive_group = [&](int lb) {
-    if (atomicAdd(d.arrive + lb, 1u) == (unsigned)s.Hkv) {
+    if (atomicAdd(d.arrive + lb, 1u) == (unsigned)s.Hkv - 1u) {
       __threadfence();   // acquire: the other arrivals' writes are visible to this CTA's selection
       s_sel[atomicAdd((int*)s_nsel, 1)] = lb;
     }
@@ -952,6 +966,22 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
     if constexpr (kFused) {
       __syncthreads();
       const int n = s_nsel[0];
+      if (n > 0 && threadIdx.x == 0 && !aborted()) {
+        // the budgets need c of the group's sequence, which the warp that
+        // completed its vocabulary chunks flags (release) once written: in
+        // the CTAs dispatched first, which wait on nothing, so this wait
+        // ends; it is bounded all the same
+        const uint32_t tag = (uint32_t)(fstep + 1);
+        bool ok = true;
+        for (int i = 0; i < n && ok; ++i) {
+          const uint32_t* f = d.conf_ready + s_sel[i] % s.B;
+          long long it = 0;
+          while (ld_acquire_gpu(f) != tag)
+            if (++it > kSpinLimit) { ok = false; break; }
+        }
+        if (!ok) fail();
+      }
+      __syncthreads();
       if (n > 0 && !aborted()) {
         __threadfence();
         SelShared& sh = *reinterpret_cast<SelShared*>(smem_raw);
@@ -1004,11 +1034,11 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
 
   // Fused step: vocabulary chunk c (sequence c / SV) by this warp.  The
   // warp that completes a sequence's chunks merges its confidence and
-  // budgets and counts one arrival on every layer of the sequence (one lane
-  // per layer).
+  // budgets and flags them (conf_ready = step + 1) for the selections.
   auto vocab_chunk = [&](int c) {
     const int bc = c / s.SV;
-    conf_partial_warp(s, d, logits, bc, c % s.SV);
+    // one round of loads for the chunk sizes of a fused step (<= 768 logits)
+    conf_partial_warp<24>(s, d, logits, bc, c % s.SV);
     unsigned int prev = 0;
     if (lane == 0) {
       __threadfence();
@@ -1020,40 +1050,42 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
       conf_merge_warp(s, d, bc, budget, conf_out);
       if (lane == 0) d.conf_done[bc] = 0u;   // zero again for the next launch
       __syncwarp();
-      __threadfence();   // the budgets and c are visible before any arrival
-      for (int ll = lane; ll < s.L; ll += 32) arrive_group(ll * s.B + bc);
+      __threadfence();   // every lane's budgets and c are visible before the flag
+      if (lane == 0) st_release_gpu(d.conf_ready + bc, (uint32_t)(fstep + 1));
     }
   };
 
+  // The work of this warp's role; every role returns here, so that the end
+  // of the CTA's work (finish: a fused step's selections) has one call site
+  // and its code one copy, fetched once per step for every warp of the CTA.
+  auto role = [&](void) {
   if constexpr (kFused) {
-    if ((int)blockIdx.x < units && warp == NC + 1) {
+    const bool vocab_cta = (int)blockIdx.x < s.vocab_ctas;
+    if (!vocab_cta && warp == NC + 1) {
       // The epilogue warp, idle until the unit is streamed, appends the new
       // token to the unit's ring slot; the proxy fence orders those stores
       // before the bulk copy (async proxy) of the ring stage that reads them
       // back, which the producer issues last, after this arrival.
-      const int u = blockIdx.x;
+      const int u = (int)blockIdx.x - s.vocab_ctas;
       const int b = (u / s.Hkv) % s.B;
       append_unit_warp<D>(s, d, u, d.T0[b] + (int)fstep, fa.k_new, fa.v_new);
       asm volatile("fence.proxy.async.global;\n" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(app_bar);
     }
-    // Vocabulary chunks.  CTAs after the units (on SMs the units leave free)
-    // reduce them with all their warps, so the confidence is merged while
-    // the units stream and no unit's epilogue warp waits for it.  With no
-    // such CTA, the epilogue warp of unit CTA c < B * SV reduces chunk c
-    // while the consumer warps stream the unit; chunks are small (512
-    // logits), so this comes before the units finish, and the last arrival
-    // of a group, with its selection, falls to the CTA of one of its units.
-    const bool vocab_cta = (int)blockIdx.x >= units;
+    // Vocabulary chunks.  The CTAs before the units (vocab_ctas of them, on
+    // SMs the units leave free, dispatched first) reduce them with all their
+    // warps, so the confidence is merged while the units stream and no
+    // unit's epilogue warp works on it.  With no such CTA, the epilogue warp
+    // of unit CTA c < B * SV reduces chunk c while the consumer warps stream
+    // the unit (small chunks: 512 logits).
     if (vocab_cta || (warp == NC + 1 && s.vocab_ctas == 0)) {
       const int nw = NTH / 32;
-      const int c0 = vocab_cta ? ((int)blockIdx.x - units) * nw + warp : (int)blockIdx.x;
+      const int c0 = vocab_cta ? (int)blockIdx.x * nw + warp : (int)blockIdx.x;
       const int stride = vocab_cta ? s.vocab_ctas * nw : s.B * s.SV;
       for (int c = c0; c < s.B * s.SV; c += stride) vocab_chunk(c);
     }
     if (vocab_cta) {
-      finish();
       return;
     }
   }
@@ -1061,14 +1093,14 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
   if (warp == NC) {
     // ------------------------------------------------ producer warp
     if constexpr (kFused) {
-      // Fused step: this CTA's one unit, u = blockIdx.x.  The header (q and
+      // Fused step: this CTA's one unit, u = blockIdx.x - vocab_ctas.  The header (q and
       // the scales) and every stage but the ring stage holding the new
       // token's slot do not depend on this step's new token; that stage
       // comes last (fused_stage), once the epilogue warp has appended the
       // token (app_bar).  The consumers read the ring positions from global
       // memory (after the ring stage's barrier), not from the header.
       const uint64_t pol = policy_evict_first();
-      const int u = blockIdx.x;
+      const int u = (int)blockIdx.x - s.vocab_ctas;
       const int h = u % s.Hkv, b = (u / s.Hkv) % s.B, l = u / (s.Hkv * s.B);
       const size_t lb = lb_index(s, l, b);
       const int nb8 = (d.n8[lb] + 15) >> 4;
@@ -1124,7 +1156,6 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
           if (!mbar_wait(full_bar(dr.slot), dr.phase)) atomicOr(d.status, kStatusTimeout);
         }
       }
-      finish();
       return;
     }
     if (lane == 0) {
@@ -1193,7 +1224,6 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
         if (!mbar_wait(full_bar(dr.slot), dr.phase)) atomicOr(d.status, kStatusTimeout);
       }
     }
-    finish();
     return;
   }
 
@@ -1202,7 +1232,6 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
     if constexpr (kFused) {
       // fused step: the append and the vocabulary chunk, if any, are done
       // (above); the consumer warps finish the unit themselves
-      finish();
       return;
     }
     // Idle until the first unit is done: the confidence of the step.
@@ -1280,7 +1309,6 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
       __syncwarp();
       if (lane == 0) mbar_arrive(efree_bar(ps));
     }
-    finish();
     return;
   }
 
@@ -1416,53 +1444,67 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
   }
   if constexpr (kFused) {
     // Fused step: the consumer warps finish this CTA's only unit, u =
-    // blockIdx.x: merge their partials, write the output and the tokens'
+    // blockIdx.x - vocab_ctas: merge their partials, write the output and the tokens'
     // attention mass (scores in shared memory), and count the unit's arrival
     // on its (layer, sequence).  Every consumer warp reaches both named
     // barriers, whether or not a bounded wait above gave up.
+    // The code here runs once per launch, so it is kept short (loops, not
+    // unrolled copies): its instructions are fetched cold every step.
     named_sync(1, NC * 32);
-    const int u = blockIdx.x;
+    const int u = (int)blockIdx.x - s.vocab_ctas;
     const int h = u % s.Hkv, b = (u / s.Hkv) % s.B, l = u / (s.Hkv * s.B);
     const size_t lb = lb_index(s, l, b);
+    const int tid = threadIdx.x;
+    const float* part = wpart;   // slot 0: [NC][G][D + 2] = o..., m, l
+    if (!aborted() && warp < G) {
+      // head warp: the maximum and normaliser over the NC partials
+      const float mw = lane < NC ? part[(lane * G + warp) * (D + 2) + D] : -INFINITY;
+      const float lw = lane < NC ? part[(lane * G + warp) * (D + 2) + D + 1] : 0.f;
+      float m = mw;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      float lsum = mw == -INFINITY ? 0.f : lw * ex2(mw - m);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+      if (lane == 0) {
+        s_stat[warp] = m;
+        s_stat[kMaxG + warp] = 1.0f / lsum;
+      }
+    }
+    named_sync(1, NC * 32);
     if (!aborted()) {
-      const int tid = threadIdx.x;
-      const float* part = wpart;   // slot 0: [NC][G][D + 2] = o..., m, l
-      float Mg[kMaxG], invL[kMaxG];
+      float* o = out + (lb * s.Hq + (size_t)h * G) * D;
+#pragma unroll 1
+      for (int idx = tid; idx < G * D; idx += NC * 32) {
+        const int gg = idx / D, c = idx - gg * D;
+        const float M = s_stat[gg];
+        float acc = 0.f;
 #pragma unroll
-      for (int gg = 0; gg < kMaxG; ++gg) {
-        Mg[gg] = 0.f;
-        invL[gg] = 0.f;
-        if (gg < G) {
-          float m = -INFINITY;
-#pragma unroll
-          for (int w = 0; w < NC; ++w) m = fmaxf(m, part[(w * G + gg) * (D + 2) + D]);
-          float lsum = 0.f;
-#pragma unroll
-          for (int w = 0; w < NC; ++w) {
-            const float mw = part[(w * G + gg) * (D + 2) + D];
-            lsum += mw == -INFINITY ? 0.f : part[(w * G + gg) * (D + 2) + D + 1] * ex2(mw - m);
-          }
-          Mg[gg] = m;
-          invL[gg] = 1.0f / lsum;
+        for (int w = 0; w < NC; ++w) {
+          const float mw = part[(w * G + gg) * (D + 2) + D];
+          if (mw != -INFINITY) acc += part[(w * G + gg) * (D + 2) + c] * ex2(mw - M);
         }
+        o[idx] = acc * s_stat[kMaxG + gg];
       }
-      // output: channel tid of every head (D <= NC * 32)
-      if (tid < D) {
-        float* o = out + (lb * s.Hq + (size_t)h * G) * D;
-#pragma unroll
-        for (int gg = 0; gg < kMaxG; ++gg) {
-          if (gg < G) {
-            float acc = 0.f;
-#pragma unroll
-            for (int w = 0; w < NC; ++w) {
-              const float mw = part[(w * G + gg) * (D + 2) + D];
-              if (mw != -INFINITY) acc += part[(w * G + gg) * (D + 2) + tid] * ex2(mw - Mg[gg]);
-            }
-            o[gg * D + tid] = acc * invL[gg];
-          }
+      // attention mass of the unit's tokens from the scores in shared memory
+      float* mass_u = d.mass + (size_t)u * s.S;
+      const int nq = (fused_nb8 * 16 + s.WR) / 4;
+#pragma unroll 1
+      for (int i = tid; i < nq; i += NC * 32) {
+        const int v = 4 * i;
+        const int slot = v < fused_nb8 * 16 ? v : s.cap + (v - fused_nb8 * 16);
+        float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+        for (int gg = 0; gg < G; ++gg) {
+          const float4 sv = *reinterpret_cast<const float4*>(scg_base + (size_t)gg * s.S + slot);
+          const float M = s_stat[gg], iL = s_stat[kMaxG + gg];
+          m.x += ex2(sv.x - M) * iL;
+          m.y += ex2(sv.y - M) * iL;
+          m.z += ex2(sv.z - M) * iL;
+          m.w += ex2(sv.w - M) * iL;
         }
+        *reinterpret_cast<float4*>(mass_u + slot) = m;
       }
-      mass_quads(u, fused_nb8, scg_base, Mg, invL, tid, NC * 32);
     }
     named_sync(1, NC * 32);
     // every consumer thread's mass stores come before the barrier; this
@@ -1473,6 +1515,8 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
       arrive_group((int)lb);
     }
   }
+  };
+  role();
   finish();
 }
 

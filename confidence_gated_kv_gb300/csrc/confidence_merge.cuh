@@ -73,10 +73,12 @@ __device__ __forceinline__ void conf_rescale(FSum& S, FSum& T, float m_old, floa
 // Partial (M, S, T, top 2) of vocabulary chunk `part` of sequence b, computed
 // by one warp in a single pass over the logits: each lane keeps its own
 // running maximum and carries its sums over when it moves, then the lanes are
-// brought to the chunk maximum and summed.  Called by all 32 lanes.
+// brought to the chunk maximum and summed.  Called by all 32 lanes.  kIn:
+// loads in flight per lane (each lane takes its elements in increasing order
+// whatever kIn is, so the result does not depend on it).
+template <int kIn = 8>
 __device__ __forceinline__ void conf_partial_warp(const Shape& s, const Dev& d,
                                                   const float* __restrict__ logits, int b, int part) {
-  constexpr int kIn = 8;   // loads in flight per lane
   const int lane = threadIdx.x & 31;
   const int V = s.V;
   const int chunk = (V + s.SV - 1) / s.SV;

@@ -146,7 +146,8 @@ struct Dev {
   int sorted;                      // prestep sorts the groups every step
   int sched;                       // how the persistent attention kernel deals its units
   uint32_t* queue;                 // next sorted position to hand out (kSchedQueue; zeroed by prestep)
-  uint32_t* arrive;                // [l*b] fused steps: units and confidence of (l, b) done this step
+  uint32_t* arrive;                // [l*b] fused steps: units of (l, b) done this step
+  uint32_t* conf_ready;            // [b] fused steps: step index + 1 once c and the budgets of b are written
 };
 
 enum : int { kSchedRoundRobin = 0, kSchedQueue = 1 };

@@ -29,14 +29,20 @@ if ROOT not in sys.path:
 
 METRIC = "CONF-KV decode steps/s (all layers) + achieved HBM GB/s vs GB300 peak, 1 GPU"
 PROFILE_EVERY = 7   # at least this many timed steps per step that records per-kernel CUDA events
+PROFILE_EVERY_LONG = 31   # the same for windows of more than PROFILE_LONG_STEPS steps
+PROFILE_LONG_STEPS = 200
 
 
-def profile_stride(pool: int) -> int:
+def profile_stride(pool: int, steps: int = 0) -> int:
     """Sampling stride for the per-kernel events: the smallest k >= PROFILE_EVERY
+    (PROFILE_EVERY_LONG for windows longer than PROFILE_LONG_STEPS steps)
     coprime with the input pool size, so that the sampled steps visit every
-    pool entry instead of a fixed subset of them."""
+    pool entry instead of a fixed subset of them.  A step that records the
+    events runs ~2-4 us longer (each event ends the launch overlap of the
+    kernels around it): 1 % of a Qwen-sized step, 10 % of an 18 us one, so
+    long windows sample more sparsely."""
     import math
-    k = PROFILE_EVERY
+    k = PROFILE_EVERY_LONG if steps > PROFILE_LONG_STEPS else PROFILE_EVERY
     while math.gcd(k, max(pool, 1)) != 1:
         k += 1
     return k
@@ -368,7 +374,7 @@ def run_ours(args):
     cfg = ck.config_from_workload(w, compaction=1 if args.compaction == "ordered" else 0)
     R = args.pool
     stream = torch.cuda.current_stream()
-    every = profile_stride(R)
+    every = profile_stride(R, args.steps)
 
     pre = untimed_steps(args.warmup, R)
     clocks = ClockSampler(local)
@@ -402,11 +408,13 @@ def run_ours(args):
         # a device delay ahead of the first event: the host queues the
         # window's first steps behind it, so the window measures the GPU
         # running the steps back to back, not the host's first launches
+        # the same confkv_step call per step, with its arguments prepared
+        # once per pool entry (host time per call stays well below a step)
+        run = cache.prepared_steps([(q[j], kn[j], vn[j], lg[j]) for j in range(R)], outs)
         torch.cuda._sleep(spin_cycles(args.steps))
         ev0.record(stream)
         for s in range(args.steps):
-            j = (pre + s) % R
-            cache.step(q[j], kn[j], vn[j], lg[j], outs)
+            run((pre + s) % R)
         ev1.record(stream)
         torch.cuda.synchronize()
         if ws > 1:

@@ -277,6 +277,27 @@ class Cache:
             raise ConfkvError(st, "confkv_step")
         return o
 
+    def prepared_steps(self, inputs, outs=None, stream=None):
+        """A decode loop over fixed device buffers: `inputs` is a list of
+        (q, k_new, v_new, logits) tensors, kept alive by the caller.  Returns
+        run(i), which makes the confkv_step call for inputs[i] with argument
+        values prepared once (no tensor indexing or pointer lookups per
+        step, which for small shapes cost more host time than the step's
+        launches)."""
+        o = self.new_outputs() if outs is None else outs
+        conf = o.get("confidence")
+        tail = (o["out"].data_ptr(), o["budget"].data_ptr(), None if conf is None else conf.data_ptr(),
+                o["evicted"].data_ptr(), o["n_evicted"].data_ptr(), _stream(stream, self._dev_index))
+        args = [(self._h, q.data_ptr(), kn.data_ptr(), vn.data_ptr(), lg.data_ptr()) + tail
+                for (q, kn, vn, lg) in inputs]
+        fn = self._fn_step
+
+        def run(i):
+            st = fn(*args[i])
+            if st != OK:
+                raise ConfkvError(st, "confkv_step")
+        return run
+
     def step_host(self, q, k_new, v_new, logits, outs, stream=None):
         """One decode step from HOST tensors (pinned for asynchronous DMA);
         outputs land in the host tensors of `outs`."""

@@ -404,12 +404,14 @@ __device__ __forceinline__ void int8_block(WarpState<D>& w, uint32_t kb, uint32_
 template <int D>
 __device__ __forceinline__ void ring_block(WarpState<D>& w, uint32_t kb, uint32_t vb,
                                            const int32_t* posb, int G, int g, int t, int lane,
-                                           float* sc_dst, float* sc_regs = nullptr) {
+                                           float* sc_dst, float* sc_regs = nullptr, int live = -1) {
+  // live: the block's slot (0-15) that holds a token whatever posb says (a
+  // fused step's new token, appended after posb was copied), or -1
   const int2 pv0 = *reinterpret_cast<const int2*>(posb + 2 * t);
   const int2 pv1 = *reinterpret_cast<const int2*>(posb + 8 + 2 * t);
   bool valid[2][2];
-  valid[0][0] = pv0.x >= 0; valid[0][1] = pv0.y >= 0;
-  valid[1][0] = pv1.x >= 0; valid[1][1] = pv1.y >= 0;
+  valid[0][0] = pv0.x >= 0 || 2 * t == live; valid[0][1] = pv0.y >= 0 || 2 * t + 1 == live;
+  valid[1][0] = pv1.x >= 0 || 8 + 2 * t == live; valid[1][1] = pv1.y >= 0 || 9 + 2 * t == live;
   float sc4[2][2];
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt) {
@@ -899,6 +901,8 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
   // fused step: the ring stage holding the new token's slot (fused_stage),
   // set by the producer before its arrival on header slot 0
   volatile int* s_jnew = s_misc + 6;
+  // fused step: the new token's ring slot (0 <= rs < WR)
+  volatile int* s_rsnew = s_misc + 7;
   // fused step: the unit's maxima Mg[kMaxG] and 1 / Lg[kMaxG]
   float* s_stat = reinterpret_cast<float*>(s_misc + 8);
   const uint32_t bar0 = smem_u32(bars);
@@ -1097,8 +1101,9 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
       // the scales) and every stage but the ring stage holding the new
       // token's slot do not depend on this step's new token; that stage
       // comes last (fused_stage), once the epilogue warp has appended the
-      // token (app_bar).  The consumers read the ring positions from global
-      // memory (after the ring stage's barrier), not from the header.
+      // token (app_bar).  The header's copy of the ring positions may hold
+      // the new token's slot before or after the append (before it, the slot
+      // is free: -1); the consumers count that slot as valid either way.
       const uint64_t pol = policy_evict_first();
       const int u = (int)blockIdx.x - s.vocab_ctas;
       const int h = u % s.Hkv, b = (u / s.Hkv) % s.B, l = u / (s.Hkv * s.B);
@@ -1134,13 +1139,16 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
       if (lane == 0) {
         s_unit[0] = u;
         s_jnew[0] = jnew;
+        s_rsnew[0] = t_new % s.WR;
         const uint32_t hdst = smem_u32(hbuf);
         const uint32_t qbytes = (uint32_t)(G * D * 2);
-        mbar_arrive_tx(hfull_bar(0), qbytes + 2u * D * 4);
+        mbar_arrive_tx(hfull_bar(0), qbytes + 2u * D * 4 + (hl.pos_in ? (uint32_t)s.WR * 4 : 0u));
         bulk_g2s(hdst + hl.q, reinterpret_cast<const char*>(q) + (lb * s.Hq + (size_t)h * G) * D * 2, qbytes,
                  hfull_bar(0));
         bulk_g2s(hdst + hl.sk, d.sK + (size_t)u * D, D * 4, hfull_bar(0));
         bulk_g2s(hdst + hl.sv, d.sV + (size_t)u * D, D * 4, hfull_bar(0));
+        if (hl.pos_in)
+          bulk_g2s(hdst + hl.pos, d.pos + lb * s.S + s.cap, (uint32_t)s.WR * 4, hfull_bar(0));
         for (int i = 0; i < sch.nst && ok; ++i) {
           if (i == sch.nst - 1 && !mbar_wait(app_bar, 0)) ok = false;
           if (ok) ok = issue(i);
@@ -1343,8 +1351,7 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
     const unsigned char* hdr = hbuf + (size_t)hs * hl.bytes;
     const float* sKh = reinterpret_cast<const float*>(hdr + hl.sk);
     const float* sVh = reinterpret_cast<const float*>(hdr + hl.sv);
-    const int32_t* posh = (hl.pos_in && !kFused) ? reinterpret_cast<const int32_t*>(hdr + hl.pos)
-                                                 : d.pos + lb * s.S + s.cap;
+    const int32_t* posh = hl.pos_in ? reinterpret_cast<const int32_t*>(hdr + hl.pos) : d.pos + lb * s.S + s.cap;
     float* scg = scg_base + (size_t)hs * G * s.S;
     Sched sch;
     sch.init(0, nb8 + nbR, nb8);
@@ -1391,8 +1398,9 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
           }
           const int rb = first + jb;
           tok0 = s.cap + rb * 16;
+          const int live = (kFused && rb == (s_rsnew[0] >> 4)) ? (s_rsnew[0] & 15) : -1;
           ring_block<D>(ws, stage + jb * 32 * D, stage + kHalf + jb * 32 * D, posh + rb * 16, G, g, t,
-                        lane, nullptr, sc4buf);
+                        lane, nullptr, sc4buf, live);
         }
       }
       __syncwarp();

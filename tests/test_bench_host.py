@@ -8,12 +8,14 @@ import bench  # noqa: E402
 
 
 def test_profile_stride_is_coprime_with_the_pool():
-    # sampled steps must visit every entry of the input pool
-    for pool in range(1, 130):
-        k = bench.profile_stride(pool)
-        assert k >= bench.PROFILE_EVERY
-        assert math.gcd(k, pool) == 1
-        assert sorted({(s * k) % pool for s in range(pool)}) == list(range(pool))
+    # sampled steps must visit every entry of the input pool, for short and
+    # long timed windows
+    for steps, least in ((20, bench.PROFILE_EVERY), (2000, bench.PROFILE_EVERY_LONG)):
+        for pool in range(1, 130):
+            k = bench.profile_stride(pool, steps)
+            assert k >= least
+            assert math.gcd(k, pool) == 1
+            assert sorted({(s * k) % pool for s in range(pool)}) == list(range(pool))
 
 
 def test_compare_policies_are_the_pages_baselines():

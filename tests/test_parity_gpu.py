@@ -285,6 +285,35 @@ def test_fused_step_with_no_sm_to_spare(mode):
     assert p.flags.evictions > 0
 
 
+def test_prepared_steps_match_step_calls():
+    # Cache.prepared_steps makes the same confkv_step calls with arguments
+    # prepared once: identical outputs and state to Cache.step
+    w = Workload(name="t_prep", B=2, L=2, Hq=8, Hkv=2, d=64, V=3000, T0=80, steps=6,
+                 n_high=(32, 32), n_low=(48, 48), P=8, W=16, q_dtype="bf16")
+    k, v = prefill_batch(w, 23, "cpu")
+    caches = []
+    for _ in range(2):
+        c = ck.Cache(ck.config_from_workload(w))
+        c.prefill(k.cuda(), v.cuda(), [w.T0] * w.B)
+        caches.append(c)
+    inputs = [tuple(x.cuda() for x in step_inputs(w, 23, s)) for s in range(6)]
+    outs = [caches[0].new_outputs(), caches[1].new_outputs()]
+    run = caches[1].prepared_steps(inputs, outs[1])
+    for s in range(6):
+        caches[0].step(*inputs[s], outs[0])
+        run(s)
+        torch.cuda.synchronize()
+        for key in ("out", "budget", "confidence", "n_evicted"):
+            assert torch.equal(outs[0][key], outs[1][key]), (s, key)
+        ne = outs[0]["n_evicted"].cpu()
+        ev0, ev1 = outs[0]["evicted"].cpu(), outs[1]["evicted"].cpu()
+        for l in range(w.L):
+            for b in range(w.B):
+                n = int(ne[l, b])   # only the first n_evicted entries of a row are written
+                assert torch.equal(ev0[l, b, :n], ev1[l, b, :n]), (s, l, b)
+    assert caches[0].stats()["evicted"] == caches[1].stats()["evicted"]
+
+
 def test_gpt2_small_batch8_pyramid_prefix():
     w = get_workload("gpt2_b8_pyramid")
     p = _run(w, 1002, 24, confident_every=6, check_state=False)

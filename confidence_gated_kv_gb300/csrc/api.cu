@@ -94,8 +94,10 @@ Shape make_shape(const confkv_config* c) {
   if (units <= sms) {
     const long long spare = sms - units;
     if (spare > 0 && spare * kFusedWarps >= (long long)c->B * ((c->V + 1023) / 1024)) {
-      s.vocab_ctas = (int)spare;
-      sv = std::max(min_sv, std::min(spare * kFusedWarps / c->B, ((long long)c->V + 255) / 256));
+      // no more CTAs than give every warp a chunk of 256 logits or more
+      const long long want = ((long long)c->B * ((c->V + 255) / 256) + kFusedWarps - 1) / kFusedWarps;
+      s.vocab_ctas = (int)std::min(spare, want);
+      sv = std::max(min_sv, std::min((long long)s.vocab_ctas * kFusedWarps / c->B, ((long long)c->V + 255) / 256));
     } else {
       int chunk = 512;
       while (chunk < 4096 && (long long)c->B * ((c->V + chunk - 1) / chunk) > units) chunk *= 2;

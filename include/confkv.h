@@ -312,10 +312,11 @@ int confkv_attention_plan(confkv_ctx* ctx, int32_t* splits, int32_t* smem_bytes)
 /* How confkv_step runs a step on the device (results do not depend on it):
  *   CONFKV_STEP_AUTO (default)  one kernel launch for the whole step when
  *       every (layer, sequence, KV head) unit can have an SM of its own
- *       (one CTA per unit), the vocabulary splits into at most one chunk
- *       per unit (chunks of 512 to 4096 logits), the INT8 region of a unit
- *       stays within 8192 tokens, compaction is tail fill, the selection's
- *       working set fits the kernel's shared memory and the logits are in
+ *       (one CTA per unit; the SMs left over reduce the vocabulary, or with
+ *       none left the units' epilogue warps take one chunk of at most 4096
+ *       logits each), the INT8 region of a unit stays within 8192 tokens,
+ *       compaction is tail fill, the selection's working set and the
+ *       unit's scores fit the kernel's shared memory and the logits are in
  *       device memory; otherwise three launches;
  *   CONFKV_STEP_SEPARATE  always three launches (confidence reduction and
  *       append; attention; selection).

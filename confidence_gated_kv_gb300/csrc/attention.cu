@@ -85,6 +85,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// One poll without the suspend hint: whether the phase has completed now.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(p) : "memory");
@@ -880,8 +891,12 @@ __device__ __forceinline__ int fused_stage(int i, int n8st, int nst, int jnew) {
 //                     The CTAs that reduce the vocabulary come first and wait
 //                     on nothing, so that wait always ends.
 //   kModeFusedDevStep the same, with the step index read from the device (a
-//                     step inside a graph reservation).
-enum : int { kModeAttention = 0, kModeFused = 1, kModeFusedDevStep = 2 };
+//                     step inside a graph reservation);
+//   kModeAttentionShared  kModeAttention for launches with few units per CTA:
+//                     the warps of a CTA share out its last unit's mass, which
+//                     would otherwise be the epilogue warp's loop alone at
+//                     the end of the kernel.
+enum : int { kModeAttention = 0, kModeFused = 1, kModeFusedDevStep = 2, kModeAttentionShared = 3 };
 
 // What a fused step needs beyond the attention arguments.
 struct FusedArgs {
@@ -899,7 +914,7 @@ struct FusedArgs {
 constexpr int kFusedSelOff = 2048;
 
 // Shared ints before the fused step's selection list (s_misc[kFusedMiscInts]).
-constexpr int kFusedMiscInts = 24;
+constexpr int kFusedMiscInts = 26;
 // Bytes of the persistent kernel's shared ints (abort flag, unit indices,
 // the fused step's selection list of up to L * B + 2 groups), a multiple of
 // 16: a fused step's score slot follows them.
@@ -908,6 +923,69 @@ __host__ __device__ inline int misc_bytes(const Shape& s) {
 }
 static_assert(sizeof(SelShared) <= kFusedSelOff, "SelShared fits below the selection area");
 
+// One quad (4 consecutive slots) of a unit's per-token attention mass:
+// mass(slot) = sum over the G query heads of 2^(s_g - M_g) / L_g, from the
+// raw-score rows scg[g * S + slot].  kStream: the scores are read once with
+// streaming loads (evict-first, coherent), so that they do not displace L1
+// lines the consumer warps use (plain cached loads here cost the kernel
+// ~8 us per launch on the Qwen-32B shape).
+template <bool kStream>
+__device__ __forceinline__ void mass_quad(float* mass_u, const float* scg, int S, int G, int slot,
+                                          const float (&Mg)[kMaxG], const float (&invL)[kMaxG]) {
+  float4 sv[kMaxG];
+#pragma unroll
+  for (int gg = 0; gg < kMaxG; ++gg) {
+    if (gg < G) {
+      const float4* src = reinterpret_cast<const float4*>(scg + (size_t)gg * S + slot);
+      sv[gg] = kStream ? __ldcs(src) : *src;
+    }
+  }
+  float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int gg = 0; gg < kMaxG; ++gg) {
+    if (gg < G) {
+      m.x += ex2(sv[gg].x - Mg[gg]) * invL[gg];
+      m.y += ex2(sv[gg].y - Mg[gg]) * invL[gg];
+      m.z += ex2(sv[gg].z - Mg[gg]) * invL[gg];
+      m.w += ex2(sv[gg].w - Mg[gg]) * invL[gg];
+    }
+  }
+  *reinterpret_cast<float4*>(mass_u + slot) = m;
+}
+
+// The mass quads of one unit (nb8 INT8 blocks, then the ring) in chunks of
+// 32, one quad per lane, taken from the shared counter *chunk until none is
+// left: the warps that share a unit this way write distinct quads.  stat
+// holds the unit's maxima M_g and 1 / L_g (kMaxG each).  The next chunk is
+// taken before the current one is written, so that the counter's round trip
+// overlaps the score loads.  Out of line: a CTA runs it once, on its last
+// unit, and it stays out of the code of the loops that run every unit.
+__device__ __noinline__ void mass_chunks_shared(float* mass_u, const float* scg, int S, int cap, int WR,
+                                                int nb8, int G, const float* stat, int* chunk) {
+  const int lane = threadIdx.x & 31;
+  float Mg[kMaxG], invL[kMaxG];
+#pragma unroll
+  for (int gg = 0; gg < kMaxG; ++gg) {
+    Mg[gg] = stat[gg];
+    invL[gg] = stat[kMaxG + gg];
+  }
+  const int nq = (nb8 * 16 + WR) / 4;
+  auto take = [&](void) {
+    int c = 0;
+    if (lane == 0) c = atomicAdd(chunk, 1);
+    return __shfl_sync(0xffffffffu, c, 0);
+  };
+  for (int c = take(); c * 32 < nq;) {
+    const int cn = take();
+    const int i = c * 32 + lane;
+    if (i < nq) {
+      const int v = 4 * i;
+      mass_quad<true>(mass_u, scg, S, G, v < nb8 * 16 ? v : cap + (v - nb8 * 16), Mg, invL);
+    }
+    c = cn;
+  }
+}
+
 template <int D, bool kFlush, int kMode, int NC>
 __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_persistent_kernel(
     Shape s, Dev d, const void* __restrict__ q, float* __restrict__ out,
@@ -915,8 +993,9 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
     int stages, FusedArgs fa) {
   static_assert(NC == 4 || NC == 8, "consumer warps");
   constexpr int NTH = (NC + 2) * 32;   // threads: NC consumer warps, the producer, the epilogue warp
-  constexpr bool kFused = kMode != kModeAttention;
+  constexpr bool kFused = kMode == kModeFused || kMode == kModeFusedDevStep;
   constexpr bool kDevStep = kMode == kModeFusedDevStep;
+  constexpr bool kShareLast = kMode == kModeAttentionShared;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   constexpr int kStageBytes = 128 * D;
   constexpr int kHalf = kStageBytes / 2;
@@ -944,8 +1023,16 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
   volatile int* s_jnew = s_misc + 6;
   // fused step: the new token's ring slot (0 <= rs < WR)
   volatile int* s_rsnew = s_misc + 7;
-  // fused step: the unit's maxima Mg[kMaxG] and 1 / Lg[kMaxG]
+  // fused step: the unit's maxima Mg[kMaxG] and 1 / Lg[kMaxG]; attention
+  // only: those of the unit whose mass is being written (s_mpub, below)
   float* s_stat = reinterpret_cast<float*>(s_misc + 8);
+  // attention only: the mass of the CTA's last unit (k-th) is shared out in
+  // chunks of 32 quads from s_mchunk, once the epilogue warp has put the
+  // unit's stats in s_stat and set s_mpub = k; the consumer warps, which
+  // have no further unit, take chunks beside it.  s_mpub = -2 - k: the
+  // epilogue writes unit k's mass alone (it did not see it was the last).
+  volatile int* s_mchunk = s_misc + 24;
+  volatile int* s_mpub = s_misc + 25;
   const uint32_t bar0 = smem_u32(bars);
   auto full_bar = [&](int i) { return bar0 + 8u * (uint32_t)i; };
   auto empty_bar = [&](int i) { return bar0 + 8u * (uint32_t)(kPMaxStages + i); };
@@ -973,6 +1060,7 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
   if (threadIdx.x == 0) {
     s_abort = 0;
     s_nsel[0] = 0;
+    s_mpub[0] = -1;
     for (int i = 0; i < stages; ++i) {
       mbar_init(full_bar(i), 1);
       mbar_init(empty_bar(i), NC);
@@ -1044,36 +1132,14 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
   // Per-token attention mass of unit u from its raw scores in score slot
   // scg, over the quads (4 consecutive slots; slot groups never straddle the
   // INT8 / ring boundary) first, first + stride, ...; empty slots get 0
-  // (never read).  The scores are read once: streaming loads (evict-first,
-  // coherent) keep them from displacing L1 lines the consumer warps use;
-  // plain cached loads here cost the kernel ~8 us per launch on the
-  // Qwen-32B shape.
+  // (never read).
   auto mass_quads = [&](int u, int nb8, const float* scg, const float (&Mg)[kMaxG], const float (&invL)[kMaxG],
                         int first, int stride) {
     float* mass_u = d.mass + (size_t)u * s.S;
     const int nq = (nb8 * 16 + s.WR) / 4;
     for (int i = first; i < nq; i += stride) {
       const int v = 4 * i;
-      const int slot = v < nb8 * 16 ? v : s.cap + (v - nb8 * 16);
-      float4 sv[kMaxG];
-#pragma unroll
-      for (int gg = 0; gg < kMaxG; ++gg) {
-        if (gg < G) {
-          const float4* src = reinterpret_cast<const float4*>(scg + (size_t)gg * s.S + slot);
-          sv[gg] = kFused ? *src : __ldcs(src);
-        }
-      }
-      float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int gg = 0; gg < kMaxG; ++gg) {
-        if (gg < G) {
-          m.x += ex2(sv[gg].x - Mg[gg]) * invL[gg];
-          m.y += ex2(sv[gg].y - Mg[gg]) * invL[gg];
-          m.z += ex2(sv[gg].z - Mg[gg]) * invL[gg];
-          m.w += ex2(sv[gg].w - Mg[gg]) * invL[gg];
-        }
-      }
-      *reinterpret_cast<float4*>(mass_u + slot) = m;
+      mass_quad<!kFused>(mass_u, scg, s.S, G, v < nb8 * 16 ? v : s.cap + (v - nb8 * 16), Mg, invL);
     }
   };
 
@@ -1349,12 +1415,37 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
           }
         }
       }
-      // attention mass of the unit's tokens
+      // attention mass of the unit's tokens.  With kShareLast, the CTA's
+      // last unit is the one whose next header the consumer warps have
+      // taken (no unit) and arrived on its done barrier (that phase cannot
+      // move on before this warp frees the slot): they share its mass.
       const float* scg = scg_base + (size_t)ps * G * s.S;
       float invL[kMaxG];
 #pragma unroll
       for (int gg = 0; gg < kMaxG; ++gg) invL[gg] = gg < G ? 1.0f / Lg[gg] : 0.f;
-      mass_quads(u, nb8, scg, Mg, invL, lane, 32);
+      int last = 0;
+      if constexpr (kShareLast) {
+        const int kn = k + 1;
+        if (lane == 0) last = mbar_test(done_bar(kn & 1), (uint32_t)((kn >> 1) & 1)) && s_eunit[kn & 1] < 0;
+        last = __shfl_sync(0xffffffffu, last, 0);
+      }
+      if (kShareLast && last) {
+        if (lane == 0) {
+          s_mchunk[0] = 0;
+#pragma unroll
+          for (int gg = 0; gg < kMaxG; ++gg) {
+            s_stat[gg] = Mg[gg];
+            s_stat[kMaxG + gg] = invL[gg];
+          }
+          __threadfence_block();
+          s_mpub[0] = k;
+        }
+        __syncwarp();
+        mass_chunks_shared(d.mass + (size_t)u * s.S, scg, s.S, s.cap, s.WR, nb8, G, s_stat, (int*)s_mchunk);
+      } else {
+        if (kShareLast && lane == 0) s_mpub[0] = -2 - k;
+        mass_quads(u, nb8, scg, Mg, invL, lane, 32);
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(efree_bar(ps));
     }
@@ -1366,7 +1457,10 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
   const uint64_t keep = policy_evict_last();
   RingPos st;
   int fused_nb8 = 0;   // fused step: INT8 blocks of the CTA's unit
-  for (int k = 0;; ++k) {
+  // k: the CTA's units so far; the loop ends on the header without a unit
+  // (every other exit aborts the CTA)
+  int k = 0;
+  for (;; ++k) {
     const int hs = k & 1;
     if (aborted() || !mbar_wait(hfull_bar(hs), (uint32_t)((k >> 1) & 1))) {
       if (!aborted()) fail();
@@ -1489,6 +1583,33 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
     if (lane == 0) {
       mbar_arrive(done_bar(hs));
       mbar_arrive(hempty_bar(hs));
+    }
+  }
+  if constexpr (kShareLast) {
+    // No further unit: take chunks of the last unit's mass beside the
+    // epilogue warp, so that the CTA's tail is not one warp's loop.  The
+    // epilogue publishes the unit's stats once the unit is done, or that it
+    // writes the mass alone (bounded wait; an aborted CTA skips this).
+    const int k_last = k - 1;
+    if (k_last >= 0 && !aborted()) {
+      int pub = 0;   // 1: help, -1: the epilogue has it
+      for (long long it = 0; it < kSpinLimit && !aborted(); ++it) {
+        const int m = s_mpub[0];
+        if (m == k_last) { pub = 1; break; }
+        if (m == -2 - k_last) { pub = -1; break; }
+        __nanosleep(64);
+      }
+      if (pub > 0) {
+        __threadfence_block();
+        // the unit and its INT8 length, as the epilogue has them
+        const int ul = s_eunit[k_last & 1];
+        const int bl = (ul / s.Hkv) % s.B, ll = ul / (s.Hkv * s.B);
+        const int nb8l = (d.n8[lb_index(s, ll, bl)] + 15) >> 4;
+        mass_chunks_shared(d.mass + (size_t)ul * s.S, scg_base + (size_t)(k_last & 1) * G * s.S, s.S, s.cap,
+                           s.WR, nb8l, G, s_stat, (int*)s_mchunk);
+      } else if (pub == 0 && !aborted()) {
+        fail();
+      }
     }
   }
   if constexpr (kFused) {
@@ -1686,6 +1807,9 @@ int launch_selftest_timeout(const Dev& d, cudaStream_t stream) {
 // INT8 tokens per unit above which the persistent kernel flushes the INT8 V
 // bias as it goes (see launch_d)
 constexpr int kFlushTokens = 8192;
+// Units per CTA below which the attention-only launch shares out each CTA's
+// last unit's mass (see launch_d)
+constexpr int kShareUnits = 8;
 
 template <int D>
 static int launch_d(const Shape& s, const Dev& d, const void* q, float* out, int32_t* budget,
@@ -1702,13 +1826,21 @@ static int launch_d(const Shape& s, const Dev& d, const void* q, float* out, int
     // blocks per warp (32K-token units), below 7e-4 up to 128.  Shorter
     // units keep the other instance: the flush state costs 2 % of a kernel
     // at its register limit (0.292 against 0.285 ms on the Qwen-32B shape).
-    static int configured[2][kMaxDevices] = {};
-    const bool flush = max_tokens - s.WR > kFlushTokens;
-    auto kern = flush ? attention_persistent_kernel<D, true, kModeAttention, kPConsumers>
-                      : attention_persistent_kernel<D, false, kModeAttention, kPConsumers>;
-    if (ensure_smem(kern, attention_max_smem(), configured[flush]) != cudaSuccess) return -1;
+    // With fewer than kShareUnits units per CTA, the instance whose warps
+    // share out a CTA's last unit's mass: there the epilogue warp's loop
+    // over that unit is a large part of the kernel's end (4K-token units, 2
+    // per CTA: 0.1118 against 0.1178 ms per launch).  With more units per
+    // CTA the last ones are the queue's shortest and the sharing code cost
+    // the kernel 1.6 % (Qwen-32B shape, 13.5 units per CTA).
+    static int configured[3][kMaxDevices] = {};
     int grid = 0, cluster = 0;
     attention_grid(s, d, 1, &grid, &cluster);
+    const bool flush = max_tokens - s.WR > kFlushTokens;
+    const bool share = !flush && units < kShareUnits * grid;
+    auto kern = flush   ? attention_persistent_kernel<D, true, kModeAttention, kPConsumers>
+                : share ? attention_persistent_kernel<D, false, kModeAttentionShared, kPConsumers>
+                        : attention_persistent_kernel<D, false, kModeAttention, kPConsumers>;
+    if (ensure_smem(kern, attention_max_smem(), configured[flush ? 1 : share ? 2 : 0]) != cudaSuccess) return -1;
     return launch_pdl(kern, dim3(grid), dim3(kPThreads), (size_t)smem, stream, s, d, q, out, budget,
                       conf_out, logits, stages_persistent(s), FusedArgs{}) == cudaSuccess
                ? 0

@@ -232,12 +232,14 @@ __device__ __forceinline__ void softmax_block(float (&sc4)[2][2], const bool (&v
                                               int G, int g, float& m_run, float& l_run,
                                               float& l_fl, float (&acc)[D / 8][4], float* sc_dst,
                                               uint32_t (&pa)[4], float* sc_regs) {
+  // Rows g >= G (padding) see q = 0, so their scores are 0: they keep a
+  // state of their own that nothing reads.
   float mloc = -INFINITY;
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
-      if (!valid[nt][j] || g >= G) sc4[nt][j] = -INFINITY;
+      if (!valid[nt][j]) sc4[nt][j] = -INFINITY;
       mloc = fmaxf(mloc, sc4[nt][j]);
     }
   // The row maximum of the four lanes exceeds m_run + 8 exactly when one
@@ -255,14 +257,15 @@ __device__ __forceinline__ void softmax_block(float (&sc4)[2][2], const bool (&v
       acc[j][0] *= corr; acc[j][1] *= corr; acc[j][2] *= corr; acc[j][3] *= corr;
     }
   }
+  // m_run is -inf only while every score of the row so far is: then any
+  // finite reference gives p = 2^(-inf) = 0 as well
+  const float m_ref = m_run == -INFINITY ? 0.f : m_run;
   float p[2][2];
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      p[nt][j] = (sc4[nt][j] == -INFINITY) ? 0.f : ex2(sc4[nt][j] - m_run);
-      l_run += p[nt][j];
-    }
+    for (int j = 0; j < 2; ++j) p[nt][j] = ex2(sc4[nt][j] - m_ref);
+  l_run += (p[0][0] + p[0][1]) + (p[1][0] + p[1][1]);
   if (sc_regs) {
     sc_regs[0] = sc4[0][0]; sc_regs[1] = sc4[0][1]; sc_regs[2] = sc4[1][0]; sc_regs[3] = sc4[1][1];
   } else if (g < G) {

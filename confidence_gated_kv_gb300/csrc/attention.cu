@@ -308,7 +308,8 @@ struct WarpState {
   float acc[D / 8][4];      // PV accumulators: rows g (hi P) and g + 8 (lo P)
   float m_run, l_run;       // reference maximum (log2 units) and lane-partial sum
   float l_flushed;          // part of l_run whose INT8 V bias is already removed
-  float qoffset;            // 1152 * sum(q') of the row (INT8 K operand offset)
+  float qoffset;            // -1152 * sum(q') / kQPre of the row: the INT8 K operand
+                            // offset, in score units and negated
   int n8blk;                // INT8 blocks done by this warp in this unit
   bool in_ring;
 };
@@ -316,7 +317,7 @@ struct WarpState {
 template <int D>
 __device__ __forceinline__ void ws_begin(WarpState<D>& w, const void* q, size_t qoff, int bf16,
                                          const float* sKu, float qs, int G, int g, int t) {
-  w.qoffset = make_q_frag<D>(w.aq, q, qoff, bf16, sKu, qs, G, g, t);
+  w.qoffset = -kQPreInv * make_q_frag<D>(w.aq, q, qoff, bf16, sKu, qs, G, g, t);
 #pragma unroll
   for (int j = 0; j < D / 8; ++j) w.acc[j][0] = w.acc[j][1] = w.acc[j][2] = w.acc[j][3] = 0.f;
   w.m_run = -INFINITY;
@@ -392,7 +393,8 @@ __device__ __forceinline__ void int8_block(WarpState<D>& w, uint32_t kb, uint32_
   for (int r = 0; r < NC; ++r) vw[r] = lds128(vb + r * 512 + lane * 16);
   float sc4[2][2];
   bool valid[2][2];
-  const bool full = blk * 16 + 16 <= n8;
+  // tokens of this lane left in the INT8 region from its first (2t)
+  const int rem = n8 - blk * 16 - 2 * t;
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt) {
     float c[4] = {0.f, 0.f, 0.f, 0.f};
@@ -402,11 +404,11 @@ __device__ __forceinline__ void int8_block(WarpState<D>& w, uint32_t kb, uint32_
       u8x4_to_h2x2_biased(comp(kw[nt * (NC / 2) + (kk >> 2)], kk & 3), b0, b1);
       mma16816(c, w.aq[kk], b0, b1);
     }
-    sc4[nt][0] = ((c[0] + c[2]) - w.qoffset) * kQPreInv;
-    sc4[nt][1] = ((c[1] + c[3]) - w.qoffset) * kQPreInv;
-    const int tok = blk * 16 + nt * 8 + 2 * t;
-    valid[nt][0] = full || tok < n8;
-    valid[nt][1] = full || tok + 1 < n8;
+    // kQPreInv is a power of two: the same value as ((c0 + c2) - 1152 sum q') / kQPre
+    sc4[nt][0] = fmaf(c[0] + c[2], kQPreInv, w.qoffset);
+    sc4[nt][1] = fmaf(c[1] + c[3], kQPreInv, w.qoffset);
+    valid[nt][0] = nt * 8 < rem;
+    valid[nt][1] = nt * 8 + 1 < rem;
   }
   uint32_t pa[4];
   softmax_block<D, kFlush>(sc4, valid, G, g, w.m_run, w.l_run, w.l_flushed, w.acc, sc_dst, pa,
@@ -1494,7 +1496,7 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
     Sched sch;
     sch.init(0, nb8 + nbR, nb8);
     WarpState<D> ws;
-    ws.qoffset = make_q_frag_s<D>(ws.aq, hdr + hl.q, s.qbf16, sKh, qs, G, g, t);
+    ws.qoffset = -kQPreInv * make_q_frag_s<D>(ws.aq, hdr + hl.q, s.qbf16, sKh, qs, G, g, t);
 #pragma unroll
     for (int j = 0; j < D / 8; ++j) ws.acc[j][0] = ws.acc[j][1] = ws.acc[j][2] = ws.acc[j][3] = 0.f;
     ws.m_run = -INFINITY;

@@ -1506,60 +1506,62 @@ __global__ void __launch_bounds__((NC + 2) * 32, NC == 4 ? 2 : 1) attention_pers
     ws.in_ring = false;
     float sc4buf[4];
     bool ok = true;
-    for (int i = 0; i < sch.nst; ++i) {
-      if (!mbar_wait(full_bar(st.slot), st.phase)) { ok = false; break; }
-      bool ring;
-      int first, nb;
-      // fused step: the producer's stage order (the new token's ring stage last)
-      sch.first_last((kFused && i >= sch.n8st) ? fused_stage(i, sch.n8st, sch.nst, s_jnew[0]) : i, ring, first,
-                     nb);
-      const uint32_t stage = smem_u32(sbuf + (size_t)st.slot * kStageBytes);
-      int tok0 = -1;
-      if (!ring) {
-        // an INT8 stage holds 4 blocks: with 8 consumer warps, warps 0-3 take
-        // the even INT8 stages and warps 4-7 the odd ones
-        const int wi = warp & 3;
-        if ((warp >> 2) == i % (NC / 4) && wi < nb) {
-          const int blk = first + wi;
-          tok0 = blk * 16;
-          int8_block<D, kFlush>(ws, stage + wi * 16 * D, stage + kHalf + wi * 16 * D, blk, n8, G, g,
-                                t, lane, nullptr, sc4buf);
-        }
+    // raw scores of tokens tok0 + {2t, 2t+1, 8+2t, 9+2t} of head g (the
+    // lane's four, in sc4buf) to the unit's score slot
+    auto store_scores = [&](int tok0) {
+      float* dst = scg + (size_t)g * s.S + tok0 + 2 * t;
+      if constexpr (kFused) {
+        // the unit's score slot in shared memory
+        *reinterpret_cast<float2*>(dst) = make_float2(sc4buf[0], sc4buf[1]);
+        *reinterpret_cast<float2*>(dst + 8) = make_float2(sc4buf[2], sc4buf[3]);
       } else {
-        // a ring stage holds 2 FP16 blocks: the warp pairs (0-1, 2-3, ...)
-        // take the ring stages in turn, so every pair works at once
-        const int jb = warp - 2 * ((i - sch.n8st) % (NC / 2));
-        if (jb >= 0 && jb < nb) {
-          if (!ws.in_ring) {
-            make_q_frag_s<D>(ws.aq, hdr + hl.q, s.qbf16, nullptr, qs, G, g, t);
-            ws.qoffset = 0.f;
-            ws_scale_v<D>(ws, sVh, t);
-            ws.in_ring = true;
-          }
-          const int rb = first + jb;
-          tok0 = s.cap + rb * 16;
-          const int live = (kFused && rb == (s_rsnew[0] >> 4)) ? (s_rsnew[0] & 15) : -1;
-          ring_block<D>(ws, stage + jb * 32 * D, stage + kHalf + jb * 32 * D, posh + rb * 16, G, g, t,
-                        lane, nullptr, sc4buf, live);
+        asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;\n" ::"l"(dst),
+                     "f"(sc4buf[0]), "f"(sc4buf[1]), "l"(keep) : "memory");
+        asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;\n" ::"l"(dst + 8),
+                     "f"(sc4buf[2]), "f"(sc4buf[3]), "l"(keep) : "memory");
+      }
+    };
+    // INT8 stages: stage i holds blocks 4i .. 4i + 3; with 8 consumer warps,
+    // warps 0-3 take the even INT8 stages and warps 4-7 the odd ones
+    for (int i = 0; i < sch.n8st; ++i) {
+      if (!mbar_wait(full_bar(st.slot), st.phase)) { ok = false; break; }
+      const uint32_t stage = smem_u32(sbuf + (size_t)st.slot * kStageBytes);
+      const int wi = warp & 3;
+      const int blk = 4 * i + wi;
+      const bool mine = (warp >> 2) == i % (NC / 4) && blk < nb8;
+      if (mine)
+        int8_block<D, kFlush>(ws, stage + wi * 16 * D, stage + kHalf + wi * 16 * D, blk, n8, G, g, t, lane,
+                              nullptr, sc4buf);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar(st.slot));
+      st.next(stages);
+      if (mine && g < G) store_scores(blk * 16);
+    }
+    // ring stages: ring stage r holds ring blocks 2r, 2r + 1; the warp
+    // pairs (0-1, 2-3, ...) take the ring stages in turn, so every pair
+    // works at once (a fused step streams the new token's stage last)
+    for (int i = sch.n8st; ok && i < sch.nst; ++i) {
+      if (!mbar_wait(full_bar(st.slot), st.phase)) { ok = false; break; }
+      const int r = (kFused ? fused_stage(i, sch.n8st, sch.nst, s_jnew[0]) : i) - sch.n8st;
+      const uint32_t stage = smem_u32(sbuf + (size_t)st.slot * kStageBytes);
+      const int jb = warp - 2 * ((i - sch.n8st) % (NC / 2));
+      const int rb = 2 * r + jb;
+      const bool mine = jb >= 0 && jb < 2 && rb < nbR;
+      if (mine) {
+        if (!ws.in_ring) {
+          make_q_frag_s<D>(ws.aq, hdr + hl.q, s.qbf16, nullptr, qs, G, g, t);
+          ws.qoffset = 0.f;
+          ws_scale_v<D>(ws, sVh, t);
+          ws.in_ring = true;
         }
+        const int live = (kFused && rb == (s_rsnew[0] >> 4)) ? (s_rsnew[0] & 15) : -1;
+        ring_block<D>(ws, stage + jb * 32 * D, stage + kHalf + jb * 32 * D, posh + rb * 16, G, g, t, lane,
+                      nullptr, sc4buf, live);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty_bar(st.slot));
       st.next(stages);
-      if (tok0 >= 0 && g < G) {
-        // raw scores of tokens tok0 + {2t, 2t+1, 8+2t, 9+2t} of head g
-        float* dst = scg + (size_t)g * s.S + tok0 + 2 * t;
-        if constexpr (kFused) {
-          // the unit's score slot in shared memory
-          *reinterpret_cast<float2*>(dst) = make_float2(sc4buf[0], sc4buf[1]);
-          *reinterpret_cast<float2*>(dst + 8) = make_float2(sc4buf[2], sc4buf[3]);
-        } else {
-          asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;\n" ::"l"(dst),
-                       "f"(sc4buf[0]), "f"(sc4buf[1]), "l"(keep) : "memory");
-          asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;\n" ::"l"(dst + 8),
-                       "f"(sc4buf[2]), "f"(sc4buf[3]), "l"(keep) : "memory");
-        }
-      }
+      if (mine && g < G) store_scores(s.cap + rb * 16);
     }
     if (!ok) {
       fail();

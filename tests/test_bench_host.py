@@ -37,15 +37,21 @@ def test_compare_policies_are_the_pages_baselines():
 def test_attention_traffic_ratio_is_read_from_the_json_record(tmp_path, monkeypatch):
     # `traffic` = this ratio x the timed launches' own algorithmic bytes; the
     # ratio comes from the machine-readable record next to the ncu summary
-    r = bench._traffic_ratio_from_profiles("attention_kernel_qwen32b")
-    assert r is not None and 1.0 <= r < 1.2
-    assert bench._traffic_ratio_from_profiles("attention_kernel_no_such_workload") is None
-    # a record marked stale (taken on a kernel that has changed since) gives none
     import json
+    with open(os.path.join(bench.ROOT, "profiles", "attention_kernel_qwen32b.json")) as f:
+        rec = json.load(f)
+    assert 1.0 <= rec["dram_bytes_per_algorithmic_byte"] < 1.2
+    r = bench._traffic_ratio_from_profiles("attention_kernel_qwen32b")
+    assert r == (None if rec.get("stale") else rec["dram_bytes_per_algorithmic_byte"])
+    assert bench._traffic_ratio_from_profiles("attention_kernel_no_such_workload") is None
     (tmp_path / "profiles").mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (tmp_path / "profiles" / "attention_kernel_x.json").write_text(
+        json.dumps({"dram_bytes_per_algorithmic_byte": 1.05, "stale": False}))
+    assert bench._traffic_ratio_from_profiles("attention_kernel_x") == 1.05
+    # a record marked stale (taken on a kernel that has changed since) gives none
     (tmp_path / "profiles" / "attention_kernel_x.json").write_text(
         json.dumps({"dram_bytes_per_algorithmic_byte": 1.05, "stale": True}))
-    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench._traffic_ratio_from_profiles("attention_kernel_x") is None
 
 
